@@ -1,0 +1,278 @@
+// gdn_recurrent.cu -- token-by-token gated delta rule for decode and speculative-verify rows.
+//
+// Semantics ("[GDN] Spec-decoding-aware attention kernel", Changes, gated_delta_rule.hpp:
+// load slot spec_state_indices[n, num_accepted[n]-1], per-token store slot
+// spec_state_indices[n, t], slot <= 0 = no prior state / no store; the non-spec rows load and
+// store state_indices[n]).  Per (token, v-head h):
+//   g = -exp(A_log[h]) softplus(a + dt_bias[h]),  beta = sigmoid(b),
+//   q^ = q / sqrt(|q|^2 + 1e-6) * scale,  k^ = k / sqrt(|k|^2 + 1e-6),
+//   S <- e^g S (I - beta k^ k^T) + beta v k^T,   o = S q^.
+// The a/b gates are read at token_indx, the same index as the q|k|v row ("[Bugfix] Align Qwen
+// GDN gates with speculative tokens", Purpose).
+//
+// GB300 design.  Decode/verify is fp32-state streaming: each (row, head) reads one 64 KiB state
+// and writes one per verify token, ~4 flops per byte, so the kernel is built for HBM, not the
+// tensor pipe.  Rows of S are independent (row i only needs s_i.k^, s_i.q^ and v_i), so one CTA
+// owns a (sequence, v-head, dv-tile of DVT rows) block and needs no cross-CTA exchange.  LPR
+// lanes share a state row, each holding DK/LPR fp32 in registers; lane l of a row takes the
+// 16-byte words l, l+LPR, l+2*LPR, ... so every warp-wide 128-bit load/store covers
+// 32*16 bytes in LPR-word runs per row.  The two dot products per token are reduced with
+// xor-shuffles inside the row's lanes, using
+//   S_t q^ = e^g (S_{t-1} q^) + delta (k^.q^),  delta = beta (v - e^g S_{t-1} k^),
+// so both reductions run on the loaded state in one pass.  The prior state is issued as
+// streaming 128-bit loads before the token data is staged, so the state fetch overlaps the
+// norm/gate prologue.  Each thread stores exactly the elements it loaded, after loading them,
+// so the load slot may also be a store slot (t = num_accepted-1) without a hazard.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+__device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_f4(float4* p, const float4& v) {
+  asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <typename ACT, typename QT, int DK, int DVT, int LPR, int TB>
+__global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) {
+  constexpr int NT = DVT * LPR;
+  constexpr int EPT = DK / LPR;  // fp32 state elements per thread
+  constexpr int NV = EPT / 4;    // float4 words per thread
+  constexpr int NWARP = NT / 32;
+  constexpr int KPL = (DK + 31) / 32;  // q/k elements per lane in the norm prologue
+  static_assert(EPT % 4 == 0 && NT % 32 == 0 && (LPR & (LPR - 1)) == 0, "bad tile");
+
+  __shared__ __align__(16) float sQ[TB][DK];
+  __shared__ __align__(16) float sK[TB][DK];
+  __shared__ float sV[TB][DVT];
+  __shared__ float sO[TB][DVT];
+  __shared__ float sEg[TB], sBeta[TB], sKQ[TB];
+  __shared__ int32_t sStore[TB], sGt[TB];
+
+  const int tid = threadIdx.x;
+  const int rr = tid / LPR;  // state row within the tile
+  const int ln = tid % LPR;  // lane within the row
+  const int h = blockIdx.y;
+  const int kh = h / (p.Hv / p.Hk);
+  const int dv0 = blockIdx.x * DVT;
+  const int z = blockIdx.z;
+  const int s = z < p.rows0 ? 0 : 1;
+  const RowsDev R = p.sub[s];
+  const int n = s == 0 ? z : z - p.rows0 + p.row_off1;
+  const bool reporter = (tid == 0 && blockIdx.x == 0 && h == 0);
+
+  const int32_t bos = __ldg(R.qsl + n), eos = __ldg(R.qsl + n + 1);
+  if (bos < 0 || eos < bos || eos > R.num_tokens) {
+    if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
+    return;
+  }
+  const int L = eos - bos;
+  if (L == 0) return;
+
+  int load_slot;
+  bool read_prior;
+  if (R.is_spec) {
+    if (L > R.spec_cols) {
+      if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
+      return;
+    }
+    const int na = __ldg(R.num_acc + n);
+    if (na < 1 || na > R.spec_cols) {
+      if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
+      return;
+    }
+    load_slot = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1);
+    read_prior = load_slot > 0;
+  } else {
+    load_slot = __ldg(R.state_idx + n);
+    read_prior = load_slot > 0 && (R.has_init == nullptr || __ldg(R.has_init + n) != 0);
+  }
+  if (load_slot >= p.num_slots) {
+    if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
+    read_prior = false;
+  }
+
+  const int64_t head_elems = (int64_t)p.dv * DK;
+  const int64_t row_off = ((int64_t)h * p.dv + dv0 + rr) * DK;  // within one slot
+  const int64_t slot_elems = (int64_t)p.Hv * head_elems;
+
+  // 1. prior state -> registers (streaming loads, issued first)
+  float4 S[NV];
+  if (read_prior) {
+    const float4* src = reinterpret_cast<const float4*>(p.ssm_pool + load_slot * slot_elems + row_off) + ln;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) S[i] = ld_stream_f4(src + i * LPR);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  const QT* __restrict__ qkv = static_cast<const QT*>(p.qkv[s]);
+  const ACT* __restrict__ ga = static_cast<const ACT*>(p.a);
+  const ACT* __restrict__ gb = static_cast<const ACT*>(p.b);
+  ACT* __restrict__ out = static_cast<ACT*>(p.out);
+  const int warp = tid / 32, lane = tid % 32;
+  const float neg_A = -expf(__ldg(p.A_log + h));
+  const float dtb = __ldg(p.dt_bias + h);
+
+  for (int tb0 = 0; tb0 < L; tb0 += TB) {
+    const int nt = min(TB, L - tb0);
+    if (tb0) __syncthreads();  // previous batch's shared data fully consumed
+
+    // 2a. per token: L2-normalised q^ (scaled), k^, k^.q^, gates, slots -- one warp per token
+    for (int t = warp; t < nt; t += NWARP) {
+      const int64_t i = bos + tb0 + t;
+      const QT* qp = qkv + i * p.C + (int64_t)kh * DK;
+      const QT* kp = qkv + i * p.C + (int64_t)p.Hk * DK + (int64_t)kh * DK;
+      float qv[KPL], kv[KPL], sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int j = 0; j < KPL; ++j) {
+        const int c = lane + 32 * j;
+        qv[j] = c < DK ? to_f32(qp[c]) : 0.f;
+        kv[j] = c < DK ? to_f32(kp[c]) : 0.f;
+        sq = fmaf(qv[j], qv[j], sq);
+        sk = fmaf(kv[j], kv[j], sk);
+      }
+      sq = warp_sum(sq);
+      sk = warp_sum(sk);
+      const float rq = 1.0f / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
+      float kq = 0.f;
+#pragma unroll
+      for (int j = 0; j < KPL; ++j) {
+        const int c = lane + 32 * j;
+        if (c < DK) {
+          const float qn = qv[j] * rq * p.scale, kn = kv[j] * rk;
+          sQ[t][c] = qn;
+          sK[t][c] = kn;
+          kq = fmaf(qn, kn, kq);
+        }
+      }
+      kq = warp_sum(kq);
+      if (lane == 0) {
+        sKQ[t] = kq;
+        const int gt = global_token(R, (int32_t)i, p.num_global, p.status);
+        sGt[t] = gt;
+        const float av = gt >= 0 ? to_f32(ga[(int64_t)gt * p.Hv + h]) : 0.f;
+        const float bv = gt >= 0 ? to_f32(gb[(int64_t)gt * p.Hv + h]) : 0.f;
+        const float xs = av + dtb;
+        const float sp = xs > 20.f ? xs : log1pf(expf(xs));
+        sEg[t] = expf(neg_A * sp);
+        sBeta[t] = 1.0f / (1.0f + expf(-bv));
+        int ss = -1;
+        if (R.is_spec) {
+          ss = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + tb0 + t);
+          if (ss >= p.num_slots) {
+            set_status(p.status, GDN_STATUS_SLOT_RANGE);
+            ss = 0;
+          }
+        }
+        sStore[t] = ss;
+      }
+    }
+    // 2b. this tile's slice of v
+    for (int idx = tid; idx < nt * DVT; idx += NT) {
+      const int t = idx / DVT, r = idx % DVT;
+      sV[t][r] = to_f32(qkv[(int64_t)(bos + tb0 + t) * p.C + 2LL * p.Hk * DK + (int64_t)h * p.dv + dv0 + r]);
+    }
+    __syncthreads();
+
+    // 3. the recurrence, token by token
+    for (int t = 0; t < nt; ++t) {
+      const float4* k4 = reinterpret_cast<const float4*>(sK[t]) + ln;
+      const float4* q4 = reinterpret_cast<const float4*>(sQ[t]) + ln;
+      float dk_ = 0.f, dq_ = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const float4 kf = k4[i * LPR], qf = q4[i * LPR];
+        dk_ = fmaf(S[i].x, kf.x, fmaf(S[i].y, kf.y, fmaf(S[i].z, kf.z, fmaf(S[i].w, kf.w, dk_))));
+        dq_ = fmaf(S[i].x, qf.x, fmaf(S[i].y, qf.y, fmaf(S[i].z, qf.z, fmaf(S[i].w, qf.w, dq_))));
+      }
+#pragma unroll
+      for (int o = LPR / 2; o >= 1; o >>= 1) {
+        dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
+        dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
+      }
+      const float eg = sEg[t], beta = sBeta[t];
+      const float delta = beta * (sV[t][rr] - eg * dk_);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const float4 kf = k4[i * LPR];
+        S[i].x = fmaf(delta, kf.x, eg * S[i].x);
+        S[i].y = fmaf(delta, kf.y, eg * S[i].y);
+        S[i].z = fmaf(delta, kf.z, eg * S[i].z);
+        S[i].w = fmaf(delta, kf.w, eg * S[i].w);
+      }
+      if (ln == 0) sO[t][rr] = fmaf(delta, sKQ[t], eg * dq_);
+      const int ss = sStore[t];
+      if (ss > 0) {
+        float4* dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off) + ln;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, S[i]);
+      }
+    }
+    __syncthreads();
+
+    // 4. outputs, scattered to the tokens' global positions
+    for (int idx = tid; idx < nt * DVT; idx += NT) {
+      const int t = idx / DVT, r = idx % DVT;
+      const int gt = sGt[t];
+      if (gt >= 0) out[((int64_t)gt * p.Hv + h) * p.dv + dv0 + r] = from_f32<ACT>(sO[t][r]);
+    }
+  }
+
+  if (!R.is_spec) {
+    const int ss = __ldg(R.state_idx + n);
+    if (ss >= p.num_slots) {
+      if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
+    } else if (ss > 0) {
+      float4* dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off) + ln;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, S[i]);
+    }
+  }
+}
+
+template <typename ACT, typename QT, int DK, int DVT>
+static cudaError_t launch_tile(const RecLaunch& p, int rows, cudaStream_t s) {
+  constexpr int LPR = 4, TB = 8;
+  const dim3 grid(p.dv / DVT, p.Hv, rows);
+  recurrent_kernel<ACT, QT, DK, DVT, LPR, TB><<<grid, DVT * LPR, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename ACT, typename QT>
+static cudaError_t launch_dk(const RecLaunch& p, int rows, cudaStream_t s) {
+  const bool t32 = (p.dv % 32) == 0;
+  switch (p.dk) {
+    case 16: return t32 ? launch_tile<ACT, QT, 16, 32>(p, rows, s) : launch_tile<ACT, QT, 16, 16>(p, rows, s);
+    case 32: return t32 ? launch_tile<ACT, QT, 32, 32>(p, rows, s) : launch_tile<ACT, QT, 32, 16>(p, rows, s);
+    case 64: return t32 ? launch_tile<ACT, QT, 64, 32>(p, rows, s) : launch_tile<ACT, QT, 64, 16>(p, rows, s);
+    case 128: return t32 ? launch_tile<ACT, QT, 128, 32>(p, rows, s) : launch_tile<ACT, QT, 128, 16>(p, rows, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_recurrent(const RecLaunch& p, gdn_dtype act, gdn_dtype qkv_dtype, int rows_total,
+                             cudaStream_t s) {
+  if (rows_total <= 0) return cudaSuccess;
+  if (act == GDN_BF16)
+    return qkv_dtype == GDN_F32 ? launch_dk<__nv_bfloat16, float>(p, rows_total, s)
+                                : launch_dk<__nv_bfloat16, __nv_bfloat16>(p, rows_total, s);
+  return qkv_dtype == GDN_F32 ? launch_dk<float, float>(p, rows_total, s)
+                              : launch_dk<float, __nv_bfloat16>(p, rows_total, s);
+}
+
+}  // namespace gdn

@@ -18,6 +18,8 @@ Row kinds follow the pages' vocabulary: ``spec`` rows verify drafts (their token
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 from typing import List, Optional
 
@@ -108,6 +110,30 @@ def _randn(shape, gen, std=1.0, dtype=torch.float32):
     return (torch.randn(shape, generator=gen, dtype=torch.float32) * std).to(dtype)
 
 
+_POOL_CHUNK = 8  # slots per independently seeded block
+
+
+def _pool_randn(shape, seed: int, tag: int, dtype) -> torch.Tensor:
+    """N(0, 1) pool [P, ...]: block j of _POOL_CHUNK slots comes from its own generator seeded
+    by (seed, tag, j), so the values do not depend on how many threads fill them."""
+    out = torch.empty(shape, dtype=dtype)
+    P = shape[0]
+    blocks = list(range(0, P, _POOL_CHUNK))
+
+    def fill(j0):
+        g = torch.Generator().manual_seed((int(seed) * 1_000_003 + int(tag) * 65_537 + j0 // _POOL_CHUNK) & 0x7FFFFFFFFFFF)
+        n = min(_POOL_CHUNK, P - j0)
+        out[j0:j0 + n] = torch.randn((n,) + tuple(shape[1:]), generator=g).to(dtype)
+
+    if len(blocks) <= 2:
+        for j0 in blocks:
+            fill(j0)
+    else:
+        with ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1))) as ex:
+            list(ex.map(fill, blocks))
+    return out
+
+
 def build_batch(layer: LayerShape, rows: List[RowSpec], *, num_slots: int, spec_cols: int = 0,
                 seed: int = 0, null_frac: float = 0.0, spec_nulls: Optional[List[tuple]] = None,
                 non_spec_nulls: Optional[List[int]] = None, shuffle_from: Optional[int] = None,
@@ -192,8 +218,8 @@ def build_batch(layer: LayerShape, rows: List[RowSpec], *, num_slots: int, spec_
     conv_b = _randn((C,), gen, 0.5, act) if conv_bias else None
     A_log = torch.log(torch.empty(Hv).uniform_(1.0, 16.0, generator=gen)).to(torch.float32)
     dt_bias = _randn((Hv,), gen, 0.1)
-    conv_pool = _randn((num_slots, SL, C), gen, 1.0, act)
-    ssm_pool = _randn((num_slots, Hv, dv, dk), gen, 1.0)
+    conv_pool = _pool_randn((num_slots, SL, C), seed, 1, act)
+    ssm_pool = _pool_randn((num_slots, Hv, dv, dk), seed, 2, torch.float32)
     x = _randn((T, C), gen, 1.0, act)
     a = _randn((T, Hv), gen, 1.0, act)
     b = _randn((T, Hv), gen, 1.0, act)
@@ -247,6 +273,18 @@ def mixed(seed: int = 3) -> Batch:
     return build_batch(big_layer(6), rows, num_slots=512, spec_cols=4, seed=seed, shuffle_from=8)
 
 
+def mixed_small(seed: int = 7) -> Batch:
+    """A small bf16 mixed batch that still spans several tiles, conv segments and ragged tails:
+    3 decode rows first, then (seeded order) 5 spec rows of up to 4 tokens -- one of them
+    ragged -- and 2 prefill rows of 70 and 130 tokens (one fresh)."""
+    layer = LayerShape(2, 4, 64, 64, 4, 6, torch.bfloat16)
+    acc = uniform_accepts(5, 4, seed + 100)
+    rows = [RowSpec("decode", 1) for _ in range(3)]
+    rows += [RowSpec("spec", 4 if i != 2 else 2, acc[i]) for i in range(5)]
+    rows += [RowSpec("prefill", 70, has_initial_state=False), RowSpec("prefill", 130)]
+    return build_batch(layer, rows, num_slots=48, spec_cols=4, seed=seed, shuffle_from=3, spec_nulls=[(1, 3)])
+
+
 def sweep_point(drafts: int, batch: int, seed: int) -> Batch:
     """Spec verify at K drafts and the given batch over a 2048-slot pool (or batch*(K+1)+1 slots
     when 2048 cannot hold distinct slots for every verify token); no NULLs."""
@@ -272,5 +310,5 @@ def ceil_div(a: int, b: int) -> int:
 
 
 __all__ = ["LayerShape", "RowSpec", "Subset", "Batch", "build_batch", "big_layer", "tiny",
-           "non_spec_decode", "spec_verify", "mixed", "sweep_point", "long_prefill",
+           "non_spec_decode", "spec_verify", "mixed", "mixed_small", "sweep_point", "long_prefill",
            "uniform_accepts", "bytes_of", "ceil_div"]

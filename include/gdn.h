@@ -1,0 +1,203 @@
+/*
+ * gdn.h -- C ABI of the Gated DeltaNet (GDN) speculative-decoding hot path on GB300 (sm_103a).
+ *
+ * The operation is the GDN linear-attention core that hybrid Qwen3-Next-style layers run when a
+ * speculative (draft + verify) step and ordinary decode/prefill rows share one batch:
+ *   (1) a width-W causal depthwise conv1d + SiLU over the packed q|k|v channels, with each
+ *       sequence's conv history kept as a rolled ring in a pool slot;
+ *   (2) the sigmoid-gated delta rule over an fp32 d_v x d_k state per v-head, with one state
+ *       slot per speculative position;
+ *   (3) the split of a mixed batch into speculative and non-speculative rows, each read from
+ *       and written back to interleaved global token positions through its own token index.
+ *
+ * Sources (page title, section):
+ *   "[GDN] Spec-decoding-aware attention kernel" (vllm-xpu-kernels PR 336) -- Problem: the conv
+ *       ring is a rolled history at column 0 of cache_indices, read at offset num_accepted-1;
+ *       Changes: the two-pass conv (stage, then a roll pass that is the slot's only writer),
+ *       the state load from spec_state_indices[n, num_accepted[n]-1], the per-token store to
+ *       spec_state_indices[n, t], slot <= 0 meaning "no prior state", and the rule that
+ *       spec_state_indices and num_accepted_tokens come as a pair.
+ *   "[XE2] Support MTP of QWEN model" (vllm-xpu-kernels PR 368) -- Copilot overview: the
+ *       spec/non-spec split, num_spec_decodes, token_indx remapping of reads and writes, the
+ *       chunked prefill path; review notes: every optional tensor is checked before use;
+ *       commit message: no rectangular assumption on spec rows, only the conservation check
+ *       non_spec_tokens + spec_tokens == num_actual_tokens.
+ *   "[Bugfix] Align Qwen GDN gates with speculative tokens" (vllm PR 51812) -- Purpose: the
+ *       a/b gates are gathered with the same index as q|k|v.
+ *
+ * Conventions shared by every entry point.
+ *   Pointers are DEVICE pointers unless stated, borrowed for the duration of the stream work;
+ *   the caller owns all memory.  Calls only enqueue work on `stream` (a cudaStream_t passed as
+ *   void*, NULL = legacy default stream); they never synchronise, never read device memory on
+ *   the host, and allocate nothing.
+ *   Dense row-major layouts, no strides.  C = 2*Hk*dk + Hv*dv packed channels ordered
+ *   q (Hk*dk) | k (Hk*dk) | v (Hv*dv), head-major.  v-head h uses k-head h / (Hv/Hk).
+ *   Activations (x, a, b, out, conv pool, conv weight/bias) use gdn_layer_desc.act_dtype.
+ *   The SSM pool is fp32 [num_slots, Hv, dv, dk] (dk fastest).  Conv pool [num_slots,
+ *   conv_state_len, C].  Slot values <= 0 are NULL: zero prior on load, no write.
+ *   Integer metadata is int32.  All activation, pool and weight pointers must be 16-byte
+ *   aligned.
+ *   Host-detectable problems return a negative gdn_error before anything is enqueued.
+ *   Problems only visible in device data (an index out of range, num_accepted outside
+ *   [1, spec_cols], a non-monotone query_start_loc, a spec row longer than spec_cols) never
+ *   trap: the kernel ORs a GDN_STATUS_* bit into *d_status (if d_status is not NULL), treats
+ *   the bad load as zero and skips the bad write (or the whole row, for row-level problems).
+ *   Rows of one call must use distinct slots; overlapping slots give undefined results.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_NULL_ARG = -1,     /* a required pointer is NULL                                   */
+  GDN_ERR_SPEC_PAIR = -2,    /* spec_state_indices without num_accepted_tokens, or vice versa */
+  GDN_ERR_SHAPE = -3,        /* head/conv sizes, spec_cols, row counts or limits unsupported  */
+  GDN_ERR_CONSERVATION = -4, /* non-spec tokens + spec tokens != num_actual_tokens            */
+  GDN_ERR_WORKSPACE = -5,    /* workspace NULL or smaller than gdn_workspace_bytes()         */
+  GDN_ERR_DTYPE = -6,        /* unknown gdn_dtype                                             */
+  GDN_ERR_CUDA = -7,         /* a kernel launch failed (cudaGetLastError after the launch)    */
+  GDN_ERR_ALIGN = -8         /* a pointer is not 16-byte aligned                              */
+} gdn_error;
+
+/* Bits ORed into *d_status by the kernels. */
+#define GDN_STATUS_SLOT_RANGE 0x1u   /* a slot index >= num_slots (load read as zero, store skipped) */
+#define GDN_STATUS_NUM_ACCEPTED 0x2u /* num_accepted_tokens[n] outside [1, spec_cols] (row skipped)  */
+#define GDN_STATUS_TOKEN_RANGE 0x4u  /* token_indx outside [0, num_global_tokens) (read zero, write skipped) */
+#define GDN_STATUS_ROW_RANGE 0x8u    /* query_start_loc not monotone / past num_tokens, or a spec row
+                                        longer than spec_cols (row skipped)                            */
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef struct {
+  int32_t num_k_heads;    /* Hk >= 1                                                   */
+  int32_t num_v_heads;    /* Hv, a multiple of Hk                                      */
+  int32_t head_k_dim;     /* dk in {16, 32, 64, 128}                                    */
+  int32_t head_v_dim;     /* dv, a multiple of 16, <= 256                               */
+  int32_t conv_width;     /* W in {2, 3, 4}                                             */
+  int32_t conv_state_len; /* columns per conv slot, >= W-1 (spec rows need >= W-2+spec_cols) */
+  gdn_dtype act_dtype;    /* GDN_BF16 or GDN_F32                                        */
+  float scale;            /* multiplies the normalised q; <= 0 selects 1/sqrt(dk)       */
+} gdn_layer_desc;
+
+typedef struct {
+  const void* conv_weight; /* [C, W] act dtype; w[c][W-1] multiplies the current token */
+  const void* conv_bias;   /* [C] act dtype, or NULL for no bias                         */
+  const float* A_log;      /* [Hv]: g = -exp(A_log[h]) * softplus(a + dt_bias[h])       */
+  const float* dt_bias;    /* [Hv]                                                       */
+} gdn_layer_params;
+
+typedef struct {
+  void* conv_pool;   /* [num_slots, conv_state_len, C] act dtype (read and written) */
+  float* ssm_pool;   /* [num_slots, Hv, dv, dk] fp32 (read and written)             */
+  int64_t num_slots; /* slot 0 is conventionally reserved as NULL                   */
+} gdn_pools;
+
+/*
+ * One subset of rows.  A subset is speculative when spec_state_indices and
+ * num_accepted_tokens are given (both, or GDN_ERR_SPEC_PAIR), otherwise non-speculative.
+ * Local tokens are numbered 0..num_tokens-1 in row order; row n owns local tokens
+ * [query_start_loc[n], query_start_loc[n+1]).
+ */
+typedef struct {
+  int32_t num_seqs;                   /* N_sub rows (may be 0)                                   */
+  int32_t num_tokens;                 /* T_sub local tokens; query_start_loc[N_sub] must equal it */
+  const int32_t* query_start_loc;     /* [N_sub+1], query_start_loc[0] == 0                       */
+  const int32_t* token_indx;          /* [T_sub] global token of each local token; NULL = identity */
+  const int32_t* state_indices;       /* non-spec: [N_sub] conv+SSM slot of each row              */
+  const int32_t* has_initial_state;   /* non-spec: [N_sub], 0 = start from zeros; NULL = all 1    */
+  const int32_t* spec_state_indices;  /* spec: [N_sub, spec_cols]; column 0 is also the conv slot */
+  const int32_t* num_accepted_tokens; /* spec: [N_sub], in [1, spec_cols]                          */
+  int32_t spec_cols;                  /* spec: columns of spec_state_indices, 1..64                */
+} gdn_rows;
+
+/*
+ * Bytes of device workspace gdn_mixed_batch (non_spec and spec as they will be passed; either
+ * may be NULL) or gdn_chunk_prefill (its rows as non_spec, spec NULL) needs.  Depends only on
+ * the host-side counts in the descriptors.  Returns 0 for invalid descriptors.
+ */
+size_t gdn_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* non_spec, const gdn_rows* spec);
+
+/*
+ * Conv update of one subset (step (1); "[GDN] Spec-decoding-aware attention kernel",
+ * Changes, causal_conv1d.hpp bullets; the review thread of "[XE2] Support MTP of QWEN model").
+ * For row n with L tokens, history h = conv_pool[slot][a : a+W-1] where
+ *   spec:     slot = spec_state_indices[n, 0], a = num_accepted_tokens[n] - 1;
+ *   non-spec: slot = state_indices[n], a = 0;
+ * h is zero when slot <= 0 or has_initial_state[n] == 0.  With H = h ++ x[token_indx[row]]:
+ *   y[t][c] = SiLU(bias[c] + sum_i conv_weight[c][i] * H[t+i][c])     (fp32 arithmetic)
+ * and, after every read of the slot, the slot's columns are rewritten as bit copies:
+ *   spec:     columns 0 .. W-3+L  <- H[1 .. W-2+L]   (column W-2+t holds token t)
+ *   non-spec: columns 0 .. W-2    <- H[L .. L+W-2]   (the last W-1 inputs)
+ * other columns and slots are untouched; slot <= 0 is not written; L = 0 rows do nothing.
+ *   x [num_global_tokens, C] act dtype (global order, gathered through token_indx);
+ *   y [rows->num_tokens, C] in y_dtype (local order).
+ */
+int gdn_conv_update(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
+                    const void* x, int32_t num_global_tokens, const gdn_rows* rows, void* y,
+                    gdn_dtype y_dtype, uint32_t* d_status, void* stream);
+
+/*
+ * Gated delta rule over one subset, token by token (step (2); "[GDN] Spec-decoding-aware
+ * attention kernel", Changes, gated_delta_rule.hpp bullet).  For v-head h of row n:
+ *   load S (dv x dk) from spec_state_indices[n, num_accepted[n]-1] (spec) or state_indices[n]
+ *   (non-spec; zeros when has_initial_state[n] == 0); zeros when the slot is <= 0;
+ *   per token: g = -exp(A_log[h]) softplus(a + dt_bias[h]) (softplus(x) = x for x > 20),
+ *   beta = sigmoid(b), q^ = q / sqrt(|q|^2 + 1e-6) * scale, k^ = k / sqrt(|k|^2 + 1e-6),
+ *   S <- e^g S (I - beta k^ k^T) + beta v k^T,  out[token_indx[i]][h] = S q^;
+ *   spec rows store S after token t to spec_state_indices[n, t]; non-spec rows store S after
+ *   their last token to state_indices[n]; slots <= 0 are not written.
+ *   qkv [rows->num_tokens, C] post-conv activation in qkv_dtype (local order);
+ *   a, b [num_global_tokens, Hv] act dtype, read at token_indx (the same index as qkv);
+ *   out [num_global_tokens, Hv, dv] act dtype, written at token_indx.
+ */
+int gdn_recurrent_step(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
+                       const void* qkv, gdn_dtype qkv_dtype, const void* a, const void* b,
+                       int32_t num_global_tokens, const gdn_rows* rows, void* out, uint32_t* d_status,
+                       void* stream);
+
+/*
+ * The same result as gdn_recurrent_step for non-speculative rows of any length, computed
+ * chunk by chunk (chunk_size tokens; 64 is the supported size) in the WY/UT form of the gated
+ * delta rule ("[XE2] Support MTP of QWEN model", Copilot overview: XE2 chunk gated delta rule
+ * with remapped output writes).  Only the final state of each row is stored.
+ *   rows must be non-speculative (GDN_ERR_SPEC_PAIR otherwise);
+ *   workspace: at least gdn_workspace_bytes(layer, rows, NULL) bytes, 256-byte aligned.
+ */
+int gdn_chunk_prefill(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
+                      const void* qkv, gdn_dtype qkv_dtype, const void* a, const void* b,
+                      int32_t num_global_tokens, const gdn_rows* rows, int32_t chunk_size, void* out,
+                      void* workspace, size_t workspace_bytes, uint32_t* d_status, void* stream);
+
+/*
+ * The whole path over a mixed batch (step (3); "[XE2] Support MTP of QWEN model", Copilot
+ * overview and commit message; "[Bugfix] Align Qwen GDN gates with speculative tokens").
+ * x [num_actual_tokens, C], a, b [num_actual_tokens, Hv] and out [num_actual_tokens, Hv, dv]
+ * are in global token order.  The non-spec subset lists num_decodes rows first, then
+ * num_prefills rows; the spec subset follows its own order.  Each subset gathers x, a and b
+ * through its own token_indx and scatters out through it; when both subsets are non-empty
+ * both token_indx must be given.  Requires
+ *   non_spec->num_tokens + spec->num_tokens == num_actual_tokens (GDN_ERR_CONSERVATION) and
+ *   num_decodes + num_prefills == non_spec->num_seqs (GDN_ERR_SHAPE).
+ * Results equal gdn_conv_update (y in fp32) followed by gdn_recurrent_step on each subset.
+ * workspace: at least gdn_workspace_bytes(layer, non_spec, spec) bytes, 256-byte aligned.
+ */
+int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
+                    const void* x, const void* a, const void* b, int32_t num_actual_tokens,
+                    const gdn_rows* non_spec, int32_t num_decodes, int32_t num_prefills, const gdn_rows* spec,
+                    void* out, void* workspace, size_t workspace_bytes, uint32_t* d_status, void* stream);
+
+/* Static text for a gdn_error value. */
+const char* gdn_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */
