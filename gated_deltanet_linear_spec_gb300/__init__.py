@@ -58,7 +58,8 @@ class _Rows(ctypes.Structure):
 
 
 EXPORTS = ("gdn_workspace_bytes", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
-           "gdn_mixed_batch", "gdn_status_string")
+           "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "gdn_status_string")
+STATIC_WORKSPACE_BYTES = 16 << 20
 
 _lib = None
 _lock = threading.Lock()
@@ -89,6 +90,9 @@ def library() -> ctypes.CDLL:
             lib.gdn_mixed_batch.restype = ctypes.c_int
             lib.gdn_mixed_batch.argtypes = [P(_LayerDesc), P(_LayerParams), P(_Pools), VP, VP, VP, I32, P(_Rows),
                                             I32, I32, P(_Rows), VP, VP, ctypes.c_size_t, VP, VP]
+            lib.gdn_mixed_batch_static_workspace.restype = ctypes.c_int
+            lib.gdn_mixed_batch_static_workspace.argtypes = [P(_LayerDesc), P(_LayerParams), P(_Pools), VP, VP, VP,
+                                                             I32, P(_Rows), I32, I32, P(_Rows), VP, VP, VP]
             _lib = lib
     return _lib
 
@@ -258,7 +262,22 @@ def gdn_mixed_batch(layer: Layer, params: Params, pools: Pools, x: torch.Tensor,
     _check(rc)
 
 
+def gdn_mixed_batch_static_workspace(layer: Layer, params: Params, pools: Pools, x: torch.Tensor, a: torch.Tensor,
+                                     b: torch.Tensor, non_spec: Optional[Rows], num_decodes: int, num_prefills: int,
+                                     spec: Optional[Rows], out: torch.Tensor, status: Optional[torch.Tensor] = None,
+                                     stream=None) -> None:
+    """gdn_mixed_batch with the library's fixed device scratch, for callers that cannot
+    allocate device memory (see include/gdn.h); allocates nothing itself."""
+    act = layer.act_dtype
+    rc = library().gdn_mixed_batch_static_workspace(
+        ctypes.byref(layer.c()), ctypes.byref(params.c(act)), ctypes.byref(pools.c(act)), _ptr(x, act, "x"),
+        _ptr(a, act, "a"), _ptr(b, act, "b"), int(x.shape[0]), _rows_ref(non_spec), int(num_decodes),
+        int(num_prefills), _rows_ref(spec), _ptr(out, act, "out"), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check(rc)
+
+
 __all__ = ["Layer", "Params", "Pools", "Rows", "GdnError", "library", "LIB_PATH", "EXPORTS",
            "gdn_workspace_bytes", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
-           "gdn_mixed_batch", "GDN_F32", "GDN_BF16", "STATUS_SLOT_RANGE", "STATUS_NUM_ACCEPTED",
+           "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "STATIC_WORKSPACE_BYTES", "GDN_F32", "GDN_BF16", "STATUS_SLOT_RANGE", "STATUS_NUM_ACCEPTED",
            "STATUS_TOKEN_RANGE", "STATUS_ROW_RANGE"]

@@ -1,0 +1,58 @@
+// gdn_static_ws.cu -- gdn_mixed_batch for callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain device scratch: a plain C host or a plugin embedded in a
+// framework that owns every device allocation and exposes no allocation hook, or a serving
+// loop that must never call cudaMalloc/cudaFree because those calls can synchronise the device
+// and stall unrelated streams.  For them this file keeps the scratch of gdn_mixed_batch (the
+// fp32 post-conv q|k|v of every token) in a fixed device array compiled into the library, so
+// the call needs nothing beyond the caller's own inputs and outputs.
+//
+// Costs and rules of the fixed array:
+//   - its GDN_STATIC_WORKSPACE_BYTES are reserved on every GPU that loads this part of the
+//     library and stay reserved until the process exits;
+//   - every call on a device shares the one array, so calls that may overlap on the GPU
+//     (different streams, or different host threads without ordering) race on it;
+//   - the array keeps whatever the previous call left; nothing in it needs to start at zero,
+//     because every element a call reads was written earlier by that same call;
+//   - in host code the array's name is only a host-side stand-in, so the device address is
+//     looked up with cudaGetSymbolAddress once per device (with that device current) on the
+//     first call made on that device; make that first call before any stream capture.
+// The paper has no counterpart to this entry point.
+#include <mutex>
+
+#include "gdn_internal.cuh"
+
+static __device__ __align__(256) unsigned char g_gdn_static_workspace[GDN_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+void* g_address[kMaxDevices] = {};
+
+// Device address of the array on the current device (looked up once per device), or NULL.
+void* static_workspace_address() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_address[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gdn_static_workspace) != cudaSuccess) return nullptr;
+    g_address[dev] = p;
+  }
+  return g_address[dev];
+}
+
+}  // namespace
+
+extern "C" int gdn_mixed_batch_static_workspace(const gdn_layer_desc* layer, const gdn_layer_params* params,
+                                                const gdn_pools* pools, const void* x, const void* a, const void* b,
+                                                int32_t num_actual_tokens, const gdn_rows* non_spec,
+                                                int32_t num_decodes, int32_t num_prefills, const gdn_rows* spec,
+                                                void* out, uint32_t* d_status, void* stream) {
+  if (gdn_workspace_bytes(layer, non_spec, spec) > (size_t)GDN_STATIC_WORKSPACE_BYTES) return GDN_ERR_WORKSPACE;
+  void* ws = static_workspace_address();
+  if (!ws) return GDN_ERR_CUDA;
+  return gdn_mixed_batch(layer, params, pools, x, a, b, num_actual_tokens, non_spec, num_decodes, num_prefills, spec,
+                         out, ws, (size_t)GDN_STATIC_WORKSPACE_BYTES, d_status, stream);
+}

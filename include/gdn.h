@@ -193,6 +193,30 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
                     const gdn_rows* non_spec, int32_t num_decodes, int32_t num_prefills, const gdn_rows* spec,
                     void* out, void* workspace, size_t workspace_bytes, uint32_t* d_status, void* stream);
 
+/*
+ * gdn_mixed_batch without a workspace argument, for callers that cannot allocate device
+ * memory: a plain C host or a plugin whose framework owns every device allocation and offers
+ * no hook for scratch, or a serving loop that must not call cudaMalloc/cudaFree because they
+ * can synchronise the device and stall other streams.  The scratch is a fixed device array of
+ * GDN_STATIC_WORKSPACE_BYTES inside the library (16 MiB: 512 tokens of an 8192-channel layer):
+ *   - it is reserved on every GPU that loads it and stays reserved until the process exits;
+ *   - every call on a device shares it, so calls that may overlap on the GPU race on it;
+ *   - it keeps the previous call's contents and is never cleared: no scratch element needs to
+ *     start at zero, every element a call reads is written earlier by the same call;
+ *   - the first call on each device looks up the array's device address with that device
+ *     current (cudaGetSymbolAddress); make that first call before any stream capture.
+ * The caller still passes inputs and outputs exactly as for gdn_mixed_batch.  Returns
+ * GDN_ERR_WORKSPACE when gdn_workspace_bytes(layer, non_spec, spec) is larger than
+ * GDN_STATIC_WORKSPACE_BYTES, GDN_ERR_CUDA when the address lookup fails, and otherwise what
+ * gdn_mixed_batch returns for the same arguments.  The paper has no counterpart to this entry point.
+ */
+#define GDN_STATIC_WORKSPACE_BYTES (16u << 20)
+int gdn_mixed_batch_static_workspace(const gdn_layer_desc* layer, const gdn_layer_params* params,
+                                     const gdn_pools* pools, const void* x, const void* a, const void* b,
+                                     int32_t num_actual_tokens, const gdn_rows* non_spec, int32_t num_decodes,
+                                     int32_t num_prefills, const gdn_rows* spec, void* out, uint32_t* d_status,
+                                     void* stream);
+
 /* Static text for a gdn_error value. */
 const char* gdn_status_string(int code);
 
