@@ -187,7 +187,7 @@ int gdn_recurrent_step(const gdn_layer_desc* layer, const gdn_layer_params* para
   r.sub[0] = rows_dev(rows);
   r.qkv[0] = qkv;
   r.rows0 = rows->num_seqs;
-  return cuda_rc(launch_recurrent(r, layer->act_dtype, qkv_dtype, rows->num_seqs, (cudaStream_t)stream));
+  return cuda_rc(launch_recurrent(r, layer->act_dtype, qkv_dtype, rows->num_seqs, false, (cudaStream_t)stream));
 }
 
 int gdn_chunk_prefill(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
@@ -252,7 +252,7 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
   r.sub[1] = rows_dev(non_spec);
   r.qkv[1] = y_ns;
   r.row_off1 = 0;
-  return cuda_rc(launch_recurrent(r, layer->act_dtype, GDN_F32, nseq(spec) + nseq(non_spec), s));
+  return cuda_rc(launch_recurrent(r, layer->act_dtype, GDN_F32, nseq(spec) + nseq(non_spec), true, s));
 }
 
 }  // extern "C"

@@ -12,12 +12,15 @@
 // GB300 design.  The pages split the update into a staging pass and a separate roll pass
 // because their work-items cover single tokens, so a row's reads and writes of its slot are
 // spread over many items.  Here one thread owns 8 channels of a row for every token it touches:
-// it loads the history into registers, runs the FMA chain over its tokens, and only then writes
-// the new columns -- the thread that reads a slot element is the only one that writes it, after
-// its read, so the roll needs no tmp buffer and no second launch.  Long non-spec rows are cut
-// into 64-token segments for parallelism; segment 0 alone touches the slot (it also fetches the
-// row's last W-1 inputs for the write-back), later segments rebuild their window from x.
-// All accesses are 16-byte vectors along the channel axis (8 bf16 or 2x4 fp32 per thread).
+// it loads the slot's history into registers before anything else, and from then on it is the
+// only reader and writer of those slot elements, so it writes the rolled columns as the tokens
+// stream through -- no tmp buffer, no second launch, no race.  Long non-spec rows are cut into
+// 64-token segments for parallelism; segment 0 alone touches the slot (it fetches the row's last
+// W-1 inputs for the write-back when the row is longer than one segment), later segments rebuild
+// their window from x.  All accesses are 16-byte vectors along the channel axis (8 bf16 or
+// 2x4 fp32 per thread); the token index and x loads of 4 tokens are issued together.
+// The kernel lets the dependent recurrence grid launch early (programmatic dependent launch):
+// that grid only reads this kernel's output after griddepcontrol.wait.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -69,17 +72,9 @@ __device__ bool locate_unit(const RowsDev& r, int unit, int& row, int& seg, uint
   return row >= 0;
 }
 
-template <int W, typename T>
-__device__ __forceinline__ Raw8<T> pick(const Raw8<T> (&h)[W - 1], int m) {
-  Raw8<T> v = h[0];
-#pragma unroll
-  for (int i = 1; i < W - 1; ++i)
-    if (i == m) v = h[i];
-  return v;
-}
-
 template <typename T, typename YT, int W>
 __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLaunch p) {
+  asm volatile("griddepcontrol.launch_dependents;");
   const int uy = blockIdx.y;
   const int s = uy < p.units0 ? 0 : 1;
   const RowsDev R = p.sub[s];
@@ -135,70 +130,99 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
 
   const T* __restrict__ x = static_cast<const T*>(p.x);
   T* __restrict__ pool = static_cast<T*>(p.conv_pool);
-  const T* __restrict__ wp = static_cast<const T*>(p.w);
   const int64_t C = p.C;
+  const int64_t slot_base = (int64_t)slot * p.state_len * C + c0;
 
+  // Weights and bias of the thread's 8 channels: 8*W contiguous elements, 16-byte vectors.
   float w[W][8], bias[8];
+  {
+    constexpr int NW = 8 * W * (int)sizeof(T) / 16;
+    uint4 wv[NW];
+    const uint4* wsrc = reinterpret_cast<const uint4*>(static_cast<const T*>(p.w) + (int64_t)c0 * W);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
+    for (int i = 0; i < NW; ++i) wv[i] = __ldg(wsrc + i);
+    const T* we = reinterpret_cast<const T*>(wv);
 #pragma unroll
-    for (int i = 0; i < W; ++i) w[i][e] = to_f32(wp[(c0 + e) * W + i]);
-    bias[e] = p.bias ? to_f32(static_cast<const T*>(p.bias)[c0 + e]) : 0.f;
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+      for (int i = 0; i < W; ++i) w[i][e] = to_f32(we[e * W + i]);
+  }
+  if (p.bias) {
+    float bb[8];
+    raw8_to_f32(load_raw8(static_cast<const T*>(p.bias) + c0), bb);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) bias[e] = bb[e];
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) bias[e] = 0.f;
   }
 
-  // Window of the W-1 inputs before the current token, and (segment 0) the raw history.
-  Raw8<T> hraw[W - 1];
-  float win[W - 1][8];
+  // Raw window of the W-1 inputs before the current token: the slot's history (segment 0)
+  // or the row's previous inputs (later segments).
+  Raw8<T> win[W - 1];
 #pragma unroll
   for (int i = 0; i < W - 1; ++i) {
     if (seg == 0) {
-      hraw[i] = read_prior ? load_raw8(pool + ((int64_t)slot * p.state_len + anchor + i) * C + c0) : zero_raw8<T>();
-      raw8_to_f32(hraw[i], win[i]);
+      win[i] = read_prior ? load_raw8(pool + slot_base + (int64_t)(anchor + i) * C) : zero_raw8<T>();
     } else {
       const int g = global_token(R, bos + t0 - (W - 1) + i, p.num_global, p.status);
-      const Raw8<T> v = g >= 0 ? load_raw8(x + (int64_t)g * C + c0) : zero_raw8<T>();
-      raw8_to_f32(v, win[i]);
-      hraw[i] = v;
+      win[i] = g >= 0 ? load_raw8(x + (int64_t)g * C + c0) : zero_raw8<T>();
     }
+  }
+  // From here on this thread owns its slot elements: every read of them is done.
+  const bool writer = (seg == 0 && slot > 0);
+  const bool spec_ring = writer && R.is_spec;
+  if (spec_ring) {
+    // spec: columns 0..W-3 <- H[1..W-2] (the shifted history); token t goes to column W-2+t below.
+#pragma unroll
+    for (int j = 0; j < W - 2; ++j) store_raw8(pool + slot_base + (int64_t)j * C, win[j + 1]);
   }
 
   YT* __restrict__ y = static_cast<YT*>(p.y[s]);
-  for (int t = t0; t < t1; ++t) {
-    const int g = global_token(R, bos + t, p.num_global, p.status);
-    float xf[8];
-    raw8_to_f32(g >= 0 ? load_raw8(x + (int64_t)g * C + c0) : zero_raw8<T>(), xf);
-    float out[8];
+  constexpr int G = 4;  // tokens whose loads are issued together
+  for (int tg = t0; tg < t1; tg += G) {
+    int gt[G];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float acc = bias[e];
+    for (int k = 0; k < G; ++k) gt[k] = (tg + k < t1) ? global_token(R, bos + tg + k, p.num_global, p.status) : -1;
+    Raw8<T> xr[G];
 #pragma unroll
-      for (int i = 0; i < W - 1; ++i) acc = fmaf(w[i][e], win[i][e], acc);
-      acc = fmaf(w[W - 1][e], xf[e], acc);
-      out[e] = acc / (1.0f + expf(-acc));
+    for (int k = 0; k < G; ++k) xr[k] = gt[k] >= 0 ? load_raw8(x + (int64_t)gt[k] * C + c0) : zero_raw8<T>();
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const int t = tg + k;
+      if (t >= t1) break;
+      float hf[W - 1][8], xf[8], out[8];
+#pragma unroll
+      for (int i = 0; i < W - 1; ++i) raw8_to_f32(win[i], hf[i]);
+      raw8_to_f32(xr[k], xf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float acc = bias[e];
+#pragma unroll
+        for (int i = 0; i < W - 1; ++i) acc = fmaf(w[i][e], hf[i][e], acc);
+        acc = fmaf(w[W - 1][e], xf[e], acc);
+        out[e] = acc / (1.0f + expf(-acc));
+      }
+      store_f32x8(y + (int64_t)(bos + t) * C + c0, out);
+      if (spec_ring) store_raw8(pool + slot_base + (int64_t)(W - 2 + t) * C, xr[k]);
+#pragma unroll
+      for (int i = 0; i < W - 2; ++i) win[i] = win[i + 1];
+      win[W - 2] = xr[k];
     }
-    store_f32x8(y + (int64_t)(bos + t) * C + c0, out);
-#pragma unroll
-    for (int i = 0; i < W - 2; ++i)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) win[i][e] = win[i + 1][e];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) win[W - 2][e] = xf[e];
   }
 
-  // Roll: this thread read its slot elements above and is their only writer.
-  if (seg == 0 && slot > 0) {
-    const int off = R.is_spec ? 1 : L;
-    const int ncols = R.is_spec ? W - 2 + L : W - 1;
-    for (int j = 0; j < ncols; ++j) {
-      const int m = off + j;
-      Raw8<T> v;
-      if (m < W - 1) {
-        v = pick<W>(hraw, m);
-      } else {
-        const int g = global_token(R, bos + m - (W - 1), p.num_global, p.status);
-        v = g >= 0 ? load_raw8(x + (int64_t)g * C + c0) : zero_raw8<T>();
+  // non-spec: columns 0..W-2 <- the row's last W-1 inputs H[L..L+W-2].
+  if (writer && !R.is_spec) {
+    if (t1 == L) {
+      // this unit saw the row's end: the window holds exactly H[L..L+W-2]
+#pragma unroll
+      for (int j = 0; j < W - 1; ++j) store_raw8(pool + slot_base + (int64_t)j * C, win[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < W - 1; ++j) {
+        const int g = global_token(R, bos + L - (W - 1) + j, p.num_global, p.status);
+        store_raw8(pool + slot_base + (int64_t)j * C, g >= 0 ? load_raw8(x + (int64_t)g * C + c0) : zero_raw8<T>());
       }
-      store_raw8(pool + ((int64_t)slot * p.state_len + j) * C + c0, v);
     }
   }
 }

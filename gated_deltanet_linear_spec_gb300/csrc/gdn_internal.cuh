@@ -153,7 +153,8 @@ struct RecLaunch {
 // Host launchers (one per kernel family); return cudaGetLastError() after the launch.
 cudaError_t launch_conv(const ConvLaunch& p, int width, gdn_dtype act, gdn_dtype y_dtype, int units_total,
                         cudaStream_t s);
-cudaError_t launch_recurrent(const RecLaunch& p, gdn_dtype act, gdn_dtype qkv_dtype, int rows_total,
+// pdl: launch as a programmatic dependent of the kernel just before it on the stream.
+cudaError_t launch_recurrent(const RecLaunch& p, gdn_dtype act, gdn_dtype qkv_dtype, int rows_total, bool pdl,
                              cudaStream_t s);
 
 }  // namespace gdn

@@ -21,23 +21,42 @@
 //   S_t q^ = e^g (S_{t-1} q^) + delta (k^.q^),  delta = beta (v - e^g S_{t-1} k^),
 // so both reductions run on the loaded state in one pass.  The prior state is issued as
 // streaming 128-bit loads before the token data is staged, so the state fetch overlaps the
-// norm/gate prologue.  Each thread stores exactly the elements it loaded, after loading them,
+// norm/gate prologue -- and, in the mixed-batch path, the tail of the conv grid, which this
+// kernel follows as a programmatic dependent launch.  Each thread stores exactly the elements it loaded, after loading them,
 // so the load slot may also be a store slot (t = num_accepted-1) without a hazard.
 #include "gdn_internal.cuh"
 
 namespace gdn {
 
+#ifndef GDN_REC_LD_HINT
+#define GDN_REC_LD_HINT 0  // 0: L1 no-allocate; 1: also ask L2 for 256-byte prefetch
+#endif
+#ifndef GDN_REC_ST_HINT
+#define GDN_REC_ST_HINT 1  // 0: default store; 1: streaming (.cs) store, evict-first in L2
+#endif
+
 __device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
   float4 v;
+#if GDN_REC_LD_HINT == 1
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+#else
   asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p));
+#endif
   return v;
 }
 
 __device__ __forceinline__ void st_f4(float4* p, const float4& v) {
+#if GDN_REC_ST_HINT == 1
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+#else
   asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                : "memory");
+#endif
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -119,6 +138,10 @@ __global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) 
 #pragma unroll
     for (int i = 0; i < NV; ++i) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+
+  // q|k|v may come from the conv grid launched just before (programmatic dependent launch):
+  // everything above touched only the state pool and metadata; wait for that grid here.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const QT* __restrict__ qkv = static_cast<const QT*>(p.qkv[s]);
   const ACT* __restrict__ ga = static_cast<const ACT*>(p.a);
@@ -245,34 +268,53 @@ __global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) 
   }
 }
 
+#ifndef GDN_REC_DVT
+#define GDN_REC_DVT 16  // state rows per CTA
+#endif
+#ifndef GDN_REC_LPR
+#define GDN_REC_LPR 8  // lanes per state row (16 fp32 each at dk = 128)
+#endif
+
 template <typename ACT, typename QT, int DK, int DVT>
-static cudaError_t launch_tile(const RecLaunch& p, int rows, cudaStream_t s) {
-  constexpr int LPR = 4, TB = 8;
-  const dim3 grid(p.dv / DVT, p.Hv, rows);
-  recurrent_kernel<ACT, QT, DK, DVT, LPR, TB><<<grid, DVT * LPR, 0, s>>>(p);
-  return cudaGetLastError();
+static cudaError_t launch_tile(const RecLaunch& p, int rows, bool pdl, cudaStream_t s) {
+  constexpr int LPR = (DK / GDN_REC_LPR >= 4) ? GDN_REC_LPR : DK / 4;
+  constexpr int TB = 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.dv / DVT, p.Hv, rows);
+  cfg.blockDim = dim3(DVT * LPR);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel<ACT, QT, DK, DVT, LPR, TB>, p);
 }
 
 template <typename ACT, typename QT>
-static cudaError_t launch_dk(const RecLaunch& p, int rows, cudaStream_t s) {
-  const bool t32 = (p.dv % 32) == 0;
+static cudaError_t launch_dk(const RecLaunch& p, int rows, bool pdl, cudaStream_t s) {
+  const bool big = (p.dv % GDN_REC_DVT) == 0;
   switch (p.dk) {
-    case 16: return t32 ? launch_tile<ACT, QT, 16, 32>(p, rows, s) : launch_tile<ACT, QT, 16, 16>(p, rows, s);
-    case 32: return t32 ? launch_tile<ACT, QT, 32, 32>(p, rows, s) : launch_tile<ACT, QT, 32, 16>(p, rows, s);
-    case 64: return t32 ? launch_tile<ACT, QT, 64, 32>(p, rows, s) : launch_tile<ACT, QT, 64, 16>(p, rows, s);
-    case 128: return t32 ? launch_tile<ACT, QT, 128, 32>(p, rows, s) : launch_tile<ACT, QT, 128, 16>(p, rows, s);
+    case 16: return big ? launch_tile<ACT, QT, 16, GDN_REC_DVT>(p, rows, pdl, s) : launch_tile<ACT, QT, 16, 16>(p, rows, pdl, s);
+    case 32: return big ? launch_tile<ACT, QT, 32, GDN_REC_DVT>(p, rows, pdl, s) : launch_tile<ACT, QT, 32, 16>(p, rows, pdl, s);
+    case 64: return big ? launch_tile<ACT, QT, 64, GDN_REC_DVT>(p, rows, pdl, s) : launch_tile<ACT, QT, 64, 16>(p, rows, pdl, s);
+    case 128: return big ? launch_tile<ACT, QT, 128, GDN_REC_DVT>(p, rows, pdl, s) : launch_tile<ACT, QT, 128, 16>(p, rows, pdl, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_recurrent(const RecLaunch& p, gdn_dtype act, gdn_dtype qkv_dtype, int rows_total,
+cudaError_t launch_recurrent(const RecLaunch& p, gdn_dtype act, gdn_dtype qkv_dtype, int rows_total, bool pdl,
                              cudaStream_t s) {
   if (rows_total <= 0) return cudaSuccess;
+  cudaError_t e;
   if (act == GDN_BF16)
-    return qkv_dtype == GDN_F32 ? launch_dk<__nv_bfloat16, float>(p, rows_total, s)
-                                : launch_dk<__nv_bfloat16, __nv_bfloat16>(p, rows_total, s);
-  return qkv_dtype == GDN_F32 ? launch_dk<float, float>(p, rows_total, s)
-                              : launch_dk<float, __nv_bfloat16>(p, rows_total, s);
+    e = qkv_dtype == GDN_F32 ? launch_dk<__nv_bfloat16, float>(p, rows_total, pdl, s)
+                             : launch_dk<__nv_bfloat16, __nv_bfloat16>(p, rows_total, pdl, s);
+  else
+    e = qkv_dtype == GDN_F32 ? launch_dk<float, float>(p, rows_total, pdl, s)
+                             : launch_dk<float, __nv_bfloat16>(p, rows_total, pdl, s);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace gdn
