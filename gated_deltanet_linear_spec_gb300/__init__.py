@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libgdn.so")
 
 GDN_F32, GDN_BF16 = 0, 1
 STATUS_SLOT_RANGE, STATUS_NUM_ACCEPTED, STATUS_TOKEN_RANGE, STATUS_ROW_RANGE = 0x1, 0x2, 0x4, 0x8
+STATUS_WAIT_TIMEOUT = 0x10
 ERRORS = {-1: "NULL_ARG", -2: "SPEC_PAIR", -3: "SHAPE", -4: "CONSERVATION", -5: "WORKSPACE",
           -6: "DTYPE", -7: "CUDA", -8: "ALIGN"}
 
@@ -57,7 +58,7 @@ class _Rows(ctypes.Structure):
                 ("spec_cols", ctypes.c_int32)]
 
 
-EXPORTS = ("gdn_workspace_bytes", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
+EXPORTS = ("gdn_workspace_bytes", "gdn_prefill_workspace_bytes", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
            "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "gdn_status_string")
 STATIC_WORKSPACE_BYTES = 16 << 20
 
@@ -78,6 +79,8 @@ def library() -> ctypes.CDLL:
             lib.gdn_status_string.argtypes = [ctypes.c_int]
             lib.gdn_workspace_bytes.restype = ctypes.c_size_t
             lib.gdn_workspace_bytes.argtypes = [P(_LayerDesc), P(_Rows), P(_Rows)]
+            lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+            lib.gdn_prefill_workspace_bytes.argtypes = [P(_LayerDesc), P(_Rows), I32]
             lib.gdn_conv_update.restype = ctypes.c_int
             lib.gdn_conv_update.argtypes = [P(_LayerDesc), P(_LayerParams), P(_Pools), VP, I32, P(_Rows), VP,
                                             ctypes.c_int, VP, VP]
@@ -209,6 +212,16 @@ def gdn_workspace_bytes(layer: Layer, non_spec: Optional[Rows], spec: Optional[R
     return int(library().gdn_workspace_bytes(ctypes.byref(layer.c()), _rows_ref(non_spec), _rows_ref(spec)))
 
 
+def gdn_prefill_workspace_bytes(layer: Layer, rows: Optional[Rows], num_prefills: int) -> int:
+    return int(library().gdn_prefill_workspace_bytes(ctypes.byref(layer.c()), _rows_ref(rows), int(num_prefills)))
+
+
+def mixed_batch_workspace_bytes(layer: Layer, non_spec: Optional[Rows], num_prefills: int,
+                                spec: Optional[Rows]) -> int:
+    """Total workspace gdn_mixed_batch needs for this batch."""
+    return gdn_workspace_bytes(layer, non_spec, spec) + gdn_prefill_workspace_bytes(layer, non_spec, num_prefills)
+
+
 def gdn_conv_update(layer: Layer, params: Params, pools: Pools, x: torch.Tensor, rows: Rows, y: torch.Tensor,
                     status: Optional[torch.Tensor] = None, stream=None) -> None:
     act = layer.act_dtype
@@ -233,7 +246,7 @@ def gdn_chunk_prefill(layer: Layer, params: Params, pools: Pools, qkv: torch.Ten
                       b: torch.Tensor, rows: Rows, out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
                       chunk_size: int = 64, status: Optional[torch.Tensor] = None, stream=None) -> None:
     act = layer.act_dtype
-    need = gdn_workspace_bytes(layer, rows, None)
+    need = gdn_prefill_workspace_bytes(layer, rows, rows.num_seqs)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
     ws_ptr = _ptr(workspace, torch.uint8, "workspace")
@@ -252,7 +265,7 @@ def gdn_mixed_batch(layer: Layer, params: Params, pools: Pools, x: torch.Tensor,
                     status: Optional[torch.Tensor] = None, stream=None) -> None:
     act = layer.act_dtype
     if workspace is None:
-        need = gdn_workspace_bytes(layer, non_spec, spec)
+        need = mixed_batch_workspace_bytes(layer, non_spec, num_prefills, spec)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     rc = library().gdn_mixed_batch(ctypes.byref(layer.c()), ctypes.byref(params.c(act)), ctypes.byref(pools.c(act)),
                                    _ptr(x, act, "x"), _ptr(a, act, "a"), _ptr(b, act, "b"), int(x.shape[0]),
@@ -278,6 +291,6 @@ def gdn_mixed_batch_static_workspace(layer: Layer, params: Params, pools: Pools,
 
 
 __all__ = ["Layer", "Params", "Pools", "Rows", "GdnError", "library", "LIB_PATH", "EXPORTS",
-           "gdn_workspace_bytes", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
+           "gdn_workspace_bytes", "gdn_prefill_workspace_bytes", "mixed_batch_workspace_bytes", "STATUS_WAIT_TIMEOUT", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
            "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "STATIC_WORKSPACE_BYTES", "GDN_F32", "GDN_BF16", "STATUS_SLOT_RANGE", "STATUS_NUM_ACCEPTED",
            "STATUS_TOKEN_RANGE", "STATUS_ROW_RANGE"]

@@ -6,6 +6,7 @@
 // kernel", Changes, gdn_attn_interface.cpp bullet), and a mixed batch only has to conserve
 // tokens, not be rectangular ("[XE2] Support MTP of QWEN model", commit message).  Nothing here
 // reads device memory, so every call is stream-ordered and can be captured in a CUDA graph.
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -79,6 +80,36 @@ int conv_units(const gdn_rows* r) {
   return (r->num_tokens + kConvSeg - 1) / kConvSeg + r->num_seqs;
 }
 
+// Chunk units of the prefill rows: an upper bound from the subset's token count.
+int prefill_units(const gdn_rows* r, int32_t num_prefills) {
+  return (r->num_tokens + kPrefillChunk - 1) / kPrefillChunk + num_prefills;
+}
+
+PrefillLaunch prefill_args(const gdn_layer_desc* d, const gdn_layer_params* prm, const gdn_pools* pools,
+                           const void* qkv, const void* a, const void* b, void* out, int32_t num_global,
+                           const gdn_rows* rows, int32_t first_row, int32_t num_rows, void* ws, uint32_t* status) {
+  PrefillLaunch p{};
+  p.qkv = qkv;
+  p.a = a;
+  p.b = b;
+  p.out = out;
+  p.num_global = num_global;
+  p.A_log = prm->A_log;
+  p.dt_bias = prm->dt_bias;
+  p.ssm_pool = pools->ssm_pool;
+  p.num_slots = pools->num_slots;
+  p.Hk = d->num_k_heads;
+  p.Hv = d->num_v_heads;
+  p.C = (int32_t)channels(d);
+  p.scale = d->scale > 0.f ? d->scale : 1.0f / sqrtf((float)d->head_k_dim);
+  p.rows = rows_dev(rows);
+  p.first_row = first_row;
+  p.num_rows = num_rows;
+  p.ws = static_cast<uint8_t*>(ws);
+  p.status = status;
+  return p;
+}
+
 float resolve_scale(const gdn_layer_desc* d) {
   return d->scale > 0.f ? d->scale : 1.0f / sqrtf((float)d->head_k_dim);
 }
@@ -138,6 +169,12 @@ const char* gdn_status_string(int code) {
     case GDN_ERR_ALIGN: return "pointer not 16-byte aligned";
     default: return "unknown gdn status";
   }
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* rows, int32_t num_prefills) {
+  if (check_layer(layer) || check_rows(layer, rows) || !rows || num_prefills <= 0) return 0;
+  if (!prefill_tc_supported(layer)) return 0;
+  return (size_t)prefill_units(rows, num_prefills) * (size_t)layer->num_v_heads * kRecBytes;
 }
 
 size_t gdn_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* non_spec, const gdn_rows* spec) {
@@ -200,11 +237,24 @@ int gdn_chunk_prefill(const gdn_layer_desc* layer, const gdn_layer_params* param
     return rc;
   if (!rows) return GDN_ERR_NULL_ARG;
   if (is_spec(rows)) return GDN_ERR_SPEC_PAIR;
-  if (chunk_size != 64) return GDN_ERR_SHAPE;
-  (void)workspace;
-  (void)workspace_bytes;
-  return gdn_recurrent_step(layer, params, pools, qkv, qkv_dtype, a, b, num_global_tokens, rows, out, d_status,
-                            stream);
+  if (chunk_size != kPrefillChunk) return GDN_ERR_SHAPE;
+  if (!prefill_tc_supported(layer))
+    return gdn_recurrent_step(layer, params, pools, qkv, qkv_dtype, a, b, num_global_tokens, rows, out, d_status,
+                              stream);
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16) return GDN_ERR_DTYPE;
+  if (rows->num_seqs == 0) return GDN_OK;
+  if (!qkv || !a || !b || !out) return GDN_ERR_NULL_ARG;
+  if (!aligned16(qkv)) return GDN_ERR_ALIGN;
+  if (num_global_tokens < 0) return GDN_ERR_SHAPE;
+  if (!rows->token_indx && rows->num_tokens > num_global_tokens) return GDN_ERR_SHAPE;
+  const size_t need = gdn_prefill_workspace_bytes(layer, rows, rows->num_seqs);
+  if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGN;
+  const int units = prefill_units(rows, rows->num_seqs);
+  if ((int64_t)units * layer->num_v_heads > (int64_t)INT32_MAX) return GDN_ERR_SHAPE;
+  PrefillLaunch p = prefill_args(layer, params, pools, qkv, a, b, out, num_global_tokens, rows, 0, rows->num_seqs,
+                                 workspace, d_status);
+  return cuda_rc(launch_prefill(p, qkv_dtype, units, (cudaStream_t)stream));
 }
 
 int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
@@ -224,13 +274,17 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
   if (num_actual_tokens == 0) return GDN_OK;
   if (!x || !a || !b || !out) return GDN_ERR_NULL_ARG;
   if (!aligned16(x)) return GDN_ERR_ALIGN;
-  const size_t need = gdn_workspace_bytes(layer, non_spec, spec);
+  // prefill rows take the tensor-core chunked path when the layer allows it
+  const bool chunked = num_prefills > 0 && prefill_tc_supported(layer);
+  const size_t base = gdn_workspace_bytes(layer, non_spec, spec);
+  const size_t need = base + (chunked ? gdn_prefill_workspace_bytes(layer, non_spec, num_prefills) : 0);
   if (need && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGN;
 
   const size_t C = (size_t)channels(layer);
   float* y_spec = static_cast<float*>(workspace);
   float* y_ns = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256((size_t)ntok(spec) * C * 4));
+  void* ws_prefill = static_cast<char*>(workspace) + base;
   cudaStream_t s = (cudaStream_t)stream;
 
   // (1) conv over both subsets in one launch: spec rows first, then the non-spec units.
@@ -244,7 +298,7 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
   if (units > 65535) return GDN_ERR_SHAPE;
   if ((rc = cuda_rc(launch_conv(c, layer->conv_width, layer->act_dtype, GDN_F32, units, s)))) return rc;
 
-  // (2) recurrence: spec rows and every non-spec row.
+  // (2) token recurrence: spec rows and the decode rows (every non-spec row when not chunked).
   RecLaunch r = rec_args(layer, params, pools, a, b, out, num_actual_tokens, d_status);
   r.sub[0] = rows_dev(spec);
   r.qkv[0] = y_spec;
@@ -252,7 +306,15 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
   r.sub[1] = rows_dev(non_spec);
   r.qkv[1] = y_ns;
   r.row_off1 = 0;
-  return cuda_rc(launch_recurrent(r, layer->act_dtype, GDN_F32, nseq(spec) + nseq(non_spec), true, s));
+  const int rec_rows = nseq(spec) + (chunked ? num_decodes : nseq(non_spec));
+  if ((rc = cuda_rc(launch_recurrent(r, layer->act_dtype, GDN_F32, rec_rows, true, s)))) return rc;
+
+  // (3) chunked prefill of the prefill rows [num_decodes, num_decodes + num_prefills).
+  if (!chunked) return GDN_OK;
+  const int chunk_units = prefill_units(non_spec, num_prefills);
+  PrefillLaunch p = prefill_args(layer, params, pools, y_ns, a, b, out, num_actual_tokens, non_spec, num_decodes,
+                                 num_prefills, ws_prefill, d_status);
+  return cuda_rc(launch_prefill(p, GDN_F32, chunk_units, s));
 }
 
 }  // extern "C"

@@ -25,53 +25,6 @@
 
 namespace gdn {
 
-// Maps work unit `unit` of a non-spec subset to (row, segment); row n owns ceil(L_n / kConvSeg)
-// units.  Warp 0 scans the rows 32 at a time; the answer is broadcast through shared memory.
-// Every thread of the block must call it.
-__device__ bool locate_unit(const RowsDev& r, int unit, int& row, int& seg, uint32_t* st) {
-  __shared__ int s_row, s_seg;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int base = 0, found_row = -1, found_seg = 0;
-    for (int r0 = 0; r0 < r.num_seqs; r0 += 32) {
-      const int n = r0 + lane;
-      int cnt = 0;
-      if (n < r.num_seqs) {
-        const int bos = __ldg(r.qsl + n), eos = __ldg(r.qsl + n + 1);
-        if (bos < 0 || eos < bos || eos > r.num_tokens) {
-          if (unit == 0) set_status(st, GDN_STATUS_ROW_RANGE);
-        } else {
-          cnt = (eos - bos + kConvSeg - 1) / kConvSeg;
-        }
-      }
-      int inc = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += v;
-      }
-      const int excl = inc - cnt;
-      const bool hit = unit >= base + excl && unit < base + inc;
-      const unsigned m = __ballot_sync(0xffffffffu, hit);
-      if (m) {
-        const int src = __ffs(m) - 1;
-        found_row = r0 + src;
-        found_seg = unit - base - __shfl_sync(0xffffffffu, excl, src);
-        break;
-      }
-      base += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (lane == 0) {
-      s_row = found_row;
-      s_seg = found_seg;
-    }
-  }
-  __syncthreads();
-  row = s_row;
-  seg = s_seg;
-  return row >= 0;
-}
-
 template <typename T, typename YT, int W>
 __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLaunch p) {
   asm volatile("griddepcontrol.launch_dependents;");
@@ -84,7 +37,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
     n = unit;
     seg = 0;
     if (n >= R.num_seqs) return;
-  } else if (!locate_unit(R, unit, n, seg, p.status)) {
+  } else if (!locate_unit(R, 0, R.num_seqs, kConvSeg, unit, n, seg, p.status)) {
     return;
   }
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;

@@ -95,6 +95,75 @@ __device__ __forceinline__ void store_f32x8(T* p, const float (&f)[8]) {
   store_raw8(p, r);
 }
 
+// ---- work units over variable-length rows ---------------------------------------------------
+
+// Units of one row: ceil(L / seg_len), 0 for empty or malformed rows.
+__device__ __forceinline__ int row_units(const RowsDev& r, int n, int seg_len, bool& bad) {
+  const int bos = __ldg(r.qsl + n), eos = __ldg(r.qsl + n + 1);
+  bad = (bos < 0 || eos < bos || eos > r.num_tokens);
+  return bad ? 0 : (eos - bos + seg_len - 1) / seg_len;
+}
+
+// Maps work unit `unit` to (row, segment) over rows [first, first + count) of r, where row n
+// owns ceil(L_n / seg_len) consecutive units in row order.  Warp 0 scans 32 rows at a time and
+// broadcasts the answer through shared memory; every thread of the block must call it.
+__device__ __forceinline__ bool locate_unit(const RowsDev& r, int first, int count, int seg_len, int unit, int& row,
+                                            int& seg, uint32_t* st) {
+  __shared__ int s_row, s_seg;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int base = 0, found_row = -1, found_seg = 0;
+    for (int r0 = 0; r0 < count; r0 += 32) {
+      int cnt = 0;
+      if (r0 + lane < count) {
+        bool bad;
+        cnt = row_units(r, first + r0 + lane, seg_len, bad);
+        if (bad && unit == 0) set_status(st, GDN_STATUS_ROW_RANGE);
+      }
+      int inc = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      const int excl = inc - cnt;
+      const unsigned m = __ballot_sync(0xffffffffu, unit >= base + excl && unit < base + inc);
+      if (m) {
+        const int src = __ffs(m) - 1;
+        found_row = first + r0 + src;
+        found_seg = unit - base - __shfl_sync(0xffffffffu, excl, src);
+        break;
+      }
+      base += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) {
+      s_row = found_row;
+      s_seg = found_seg;
+    }
+  }
+  __syncthreads();
+  row = s_row;
+  seg = s_seg;
+  return row >= 0;
+}
+
+// Units owned by rows [first, n): the index of row n's first unit.  Every thread must call it.
+__device__ __forceinline__ int units_before(const RowsDev& r, int first, int n, int seg_len) {
+  __shared__ int s_sum;
+  if (threadIdx.x < 32) {
+    int acc = 0;
+    for (int m = first + (int)threadIdx.x; m < n; m += 32) {
+      bool bad;
+      acc += row_units(r, m, seg_len, bad);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (threadIdx.x == 0) s_sum = acc;
+  }
+  __syncthreads();
+  return s_sum;
+}
+
 // ---- launch plumbing (host) ----------------------------------------------------------------
 
 inline RowsDev rows_dev(const gdn_rows* r) {
@@ -150,11 +219,37 @@ struct RecLaunch {
   uint32_t* status;
 };
 
+// Chunked prefill (tensor-core path): chunk length and the per (chunk, v-head) record size.
+constexpr int kPrefillChunk = 64;
+constexpr uint32_t kRecBytes = 123904;
+
+struct PrefillLaunch {
+  const void* qkv;  // post-conv q|k|v [T_sub, C] (fp32 or bf16), local order
+  const void* a;
+  const void* b;
+  void* out;
+  int32_t num_global;
+  const float* A_log;
+  const float* dt_bias;
+  float* ssm_pool;
+  int64_t num_slots;
+  int32_t Hk, Hv, C;
+  float scale;
+  RowsDev rows;       // a non-spec subset
+  int32_t first_row;  // the prefill rows are [first_row, first_row + num_rows)
+  int32_t num_rows;
+  uint8_t* ws;        // units x Hv records of kRecBytes
+  uint32_t* status;
+};
+
 // Host launchers (one per kernel family); return cudaGetLastError() after the launch.
 cudaError_t launch_conv(const ConvLaunch& p, int width, gdn_dtype act, gdn_dtype y_dtype, int units_total,
                         cudaStream_t s);
 // pdl: launch as a programmatic dependent of the kernel just before it on the stream.
 cudaError_t launch_recurrent(const RecLaunch& p, gdn_dtype act, gdn_dtype qkv_dtype, int rows_total, bool pdl,
                              cudaStream_t s);
+// The tensor-core chunked prefill handles dk = dv = 128 with bf16 activations.
+bool prefill_tc_supported(const gdn_layer_desc* d);
+cudaError_t launch_prefill(const PrefillLaunch& p, gdn_dtype qkv_dtype, int units_upper, cudaStream_t s);
 
 }  // namespace gdn

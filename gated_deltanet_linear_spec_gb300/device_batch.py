@@ -6,7 +6,7 @@ from typing import Optional
 
 import torch
 
-from . import Layer, Params, Pools, Rows, gdn_mixed_batch, gdn_workspace_bytes
+from . import Layer, Params, Pools, Rows, gdn_mixed_batch, mixed_batch_workspace_bytes
 from .workloads import Batch, Subset
 
 
@@ -52,7 +52,8 @@ def to_device(batch: Batch, device="cuda", pools: Optional[Pools] = None) -> Dev
     spec, non_spec = rows_to_device(batch.spec, device), rows_to_device(batch.non_spec, device)
     T = batch.num_actual_tokens
     out = torch.zeros((T, L.num_v_heads, L.head_v_dim), dtype=L.act_dtype, device=device)
-    ws = torch.empty(max(1, gdn_workspace_bytes(layer, non_spec, spec)), dtype=torch.uint8, device=device)
+    ws = torch.empty(max(1, mixed_batch_workspace_bytes(layer, non_spec, batch.num_prefills, spec)),
+                     dtype=torch.uint8, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
     return DeviceBatch(layer, params, pools, dev(batch.x), dev(batch.a), dev(batch.b), spec, non_spec,
                        batch.num_decodes, batch.num_prefills, out, ws, status)

@@ -274,10 +274,11 @@ def mixed(seed: int = 3) -> Batch:
 
 
 def mixed_small(seed: int = 7) -> Batch:
-    """A small bf16 mixed batch that still spans several tiles, conv segments and ragged tails:
-    3 decode rows first, then (seeded order) 5 spec rows of up to 4 tokens -- one of them
-    ragged -- and 2 prefill rows of 70 and 130 tokens (one fresh)."""
-    layer = LayerShape(2, 4, 64, 64, 4, 6, torch.bfloat16)
+    """A small bf16 mixed batch (1 k-head, 2 v-heads of 128) that still spans several tiles,
+    conv segments, chunks and ragged tails: 3 decode rows first, then (seeded order) 5 spec rows
+    of up to 4 tokens -- one of them ragged -- and 2 prefill rows of 70 and 130 tokens (one
+    fresh)."""
+    layer = LayerShape(1, 2, 128, 128, 4, 6, torch.bfloat16)
     acc = uniform_accepts(5, 4, seed + 100)
     rows = [RowSpec("decode", 1) for _ in range(3)]
     rows += [RowSpec("spec", 4 if i != 2 else 2, acc[i]) for i in range(5)]

@@ -72,6 +72,8 @@ typedef enum {
 #define GDN_STATUS_TOKEN_RANGE 0x4u  /* token_indx outside [0, num_global_tokens) (read zero, write skipped) */
 #define GDN_STATUS_ROW_RANGE 0x8u    /* query_start_loc not monotone / past num_tokens, or a spec row
                                         longer than spec_cols (row skipped)                            */
+#define GDN_STATUS_WAIT_TIMEOUT 0x10u /* a bounded wait inside a tensor-core kernel gave up; that
+                                         block's results are missing (never expected in practice)  */
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
@@ -118,11 +120,21 @@ typedef struct {
 } gdn_rows;
 
 /*
- * Bytes of device workspace gdn_mixed_batch (non_spec and spec as they will be passed; either
- * may be NULL) or gdn_chunk_prefill (its rows as non_spec, spec NULL) needs.  Depends only on
- * the host-side counts in the descriptors.  Returns 0 for invalid descriptors.
+ * Bytes of device workspace gdn_mixed_batch needs for a batch without prefill rows (non_spec
+ * and spec as they will be passed; either may be NULL): the fp32 post-conv q|k|v of every token.
+ * Depends only on the host-side counts in the descriptors.  Returns 0 for invalid descriptors.
  */
 size_t gdn_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* non_spec, const gdn_rows* spec);
+
+/*
+ * Extra workspace the chunked prefill needs when `rows` (a non-spec subset) holds num_prefills
+ * prefill rows: one record per (64-token chunk, v-head), bounded from rows->num_tokens and
+ * num_prefills.  gdn_mixed_batch needs gdn_workspace_bytes() + gdn_prefill_workspace_bytes(
+ * layer, non_spec, num_prefills); gdn_chunk_prefill needs gdn_prefill_workspace_bytes(layer,
+ * rows, rows->num_seqs).  0 when the layer does not take the tensor-core path (see
+ * gdn_chunk_prefill) or num_prefills is 0.
+ */
+size_t gdn_prefill_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* rows, int32_t num_prefills);
 
 /*
  * Conv update of one subset (step (1); "[GDN] Spec-decoding-aware attention kernel",
@@ -165,10 +177,13 @@ int gdn_recurrent_step(const gdn_layer_desc* layer, const gdn_layer_params* para
 /*
  * The same result as gdn_recurrent_step for non-speculative rows of any length, computed
  * chunk by chunk (chunk_size tokens; 64 is the supported size) in the WY/UT form of the gated
- * delta rule ("[XE2] Support MTP of QWEN model", Copilot overview: XE2 chunk gated delta rule
- * with remapped output writes).  Only the final state of each row is stored.
+ * delta rule on tcgen05 tensor cores ("[XE2] Support MTP of QWEN model", Copilot overview: XE2
+ * chunk gated delta rule with remapped output writes).  Only the final state of each row is
+ * stored.  The tensor-core path covers dk = dv = 128 with bf16 activations; other layers run the
+ * token recurrence of gdn_recurrent_step (and need no workspace).
  *   rows must be non-speculative (GDN_ERR_SPEC_PAIR otherwise);
- *   workspace: at least gdn_workspace_bytes(layer, rows, NULL) bytes, 256-byte aligned.
+ *   workspace: at least gdn_prefill_workspace_bytes(layer, rows, rows->num_seqs) bytes,
+ *   256-byte aligned (may be NULL when that is 0).
  */
 int gdn_chunk_prefill(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
                       const void* qkv, gdn_dtype qkv_dtype, const void* a, const void* b,
@@ -185,8 +200,10 @@ int gdn_chunk_prefill(const gdn_layer_desc* layer, const gdn_layer_params* param
  * both token_indx must be given.  Requires
  *   non_spec->num_tokens + spec->num_tokens == num_actual_tokens (GDN_ERR_CONSERVATION) and
  *   num_decodes + num_prefills == non_spec->num_seqs (GDN_ERR_SHAPE).
- * Results equal gdn_conv_update (y in fp32) followed by gdn_recurrent_step on each subset.
- * workspace: at least gdn_workspace_bytes(layer, non_spec, spec) bytes, 256-byte aligned.
+ * Results equal gdn_conv_update (y in fp32) followed by gdn_recurrent_step on the spec rows and
+ * the decode rows, and gdn_chunk_prefill on the prefill rows.
+ * workspace: at least gdn_workspace_bytes(layer, non_spec, spec) +
+ * gdn_prefill_workspace_bytes(layer, non_spec, num_prefills) bytes, 256-byte aligned.
  */
 int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
                     const void* x, const void* a, const void* b, int32_t num_actual_tokens,

@@ -119,14 +119,28 @@ def test_random_interleavings_of_a_mixed_batch(seed):
 
 
 def test_mixed_call_equals_one_call_per_subset():
+    """gdn_mixed_batch == conv per subset, then the token recurrence on spec and decode rows and
+    the chunked prefill on the prefill rows, bit for bit."""
     batch = W.mixed_small(5)
     whole = run_gpu(batch)
     d = to_device(batch)
     C = batch.layer.channels
-    for rows in (d.spec, d.non_spec):
-        y = torch.empty((rows.num_tokens, C), dtype=torch.float32, device="cuda")
-        gdn.gdn_conv_update(d.layer, d.params, d.pools, d.x, rows, y, d.status)
-        gdn.gdn_recurrent_step(d.layer, d.params, d.pools, y, d.a, d.b, rows, d.out, d.status)
+    ys = {}
+    for name, rows in (("spec", d.spec), ("non_spec", d.non_spec)):
+        ys[name] = torch.empty((rows.num_tokens, C), dtype=torch.float32, device="cuda")
+        gdn.gdn_conv_update(d.layer, d.params, d.pools, d.x, rows, ys[name], d.status)
+    gdn.gdn_recurrent_step(d.layer, d.params, d.pools, ys["spec"], d.a, d.b, d.spec, d.out, d.status)
+    ns, nd = d.non_spec, batch.num_decodes
+    q = ns.query_start_loc
+    split = int(q[nd])
+    dec = gdn.Rows(q[: nd + 1].contiguous(), split, ns.token_indx[:split].contiguous(),
+                   ns.state_indices[:nd].contiguous(), ns.has_initial_state[:nd].contiguous())
+    pre = gdn.Rows((q[nd:] - split).contiguous(), ns.num_tokens - split, ns.token_indx[split:].contiguous(),
+                   ns.state_indices[nd:].contiguous(), ns.has_initial_state[nd:].contiguous())
+    gdn.gdn_recurrent_step(d.layer, d.params, d.pools, ys["non_spec"][:split].contiguous(), d.a, d.b, dec, d.out,
+                           d.status)
+    gdn.gdn_chunk_prefill(d.layer, d.params, d.pools, ys["non_spec"][split:].contiguous(), d.a, d.b, pre, d.out,
+                          status=d.status)
     torch.cuda.synchronize()
     assert int(d.status.item()) == 0
     assert np.array_equal(np_act(d.out.cpu()), whole.out)
