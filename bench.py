@@ -37,7 +37,46 @@ UNIT = "tokens/s"
 WORKLOAD = ("spec_verify: 1 GDN layer Hk=16 Hv=32 dk=dv=128, conv width 4 over 8192 bf16 channels, fp32 state; "
             "64 rows x 4 verify tokens (3 drafts), num_accepted U[1,4], 512-slot pool, 5% NULL slots")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+
+# Other workloads (parity configurations) can be timed for profiling; the metric's line is spec_verify.
+WORKLOADS = {
+    "spec_verify": WORKLOAD,
+    "non_spec_decode": "non_spec_decode: same layer, 64 one-token non-spec rows, 256-slot pool",
+    "mixed": "mixed: same layer, 8 decode rows first, 32 spec rows of 4 tokens and prefill rows of 512 and 1024 "
+             "tokens interleaved",
+    "long_prefill": "long_prefill: same layer, one 8192-token prefill row continuing a prior state",
+}
+
+
+def make_workload(name):
+    from gated_deltanet_linear_spec_gb300 import workloads
+    return {"spec_verify": workloads.spec_verify, "non_spec_decode": workloads.non_spec_decode,
+            "mixed": workloads.mixed, "long_prefill": lambda: workloads.long_prefill(8192)}[name]()
+
+
+def source_hash(*names) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_spec_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this exact source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload \
+                    and parts[2] == src_hash:
+                return int(parts[3])
+    return None
 
 
 def measured_peaks() -> dict:
@@ -140,29 +179,75 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------
 # the CPU oracle (reference arm and cpu_baseline)
 
-def oracle_tokens_per_s(batch, budget_s: float = 12.0) -> dict:
+def oracle_tokens_per_s(batch, budget_s: float = 12.0, heads=None) -> dict:
+    """The CPU oracle as it stands, timed on this host's cores over a bounded sample: the whole
+    workload (or a few v-heads of it, scaled to all heads), repeated until budget_s has passed."""
     from tests.oracle_run import np_act, run_oracle
     cores = len(os.sched_getaffinity(0))
     conv_pool, ssm_pool = np_act(batch.conv_pool), np_act(batch.ssm_pool)  # copied once, outside the timing
+    Hv = batch.layer.num_v_heads
+    frac = 1.0 if heads is None else (heads[1] - heads[0]) / Hv
     reps, el = 0, 0.0
-    while el < budget_s and reps < 50:
+    while el < budget_s and reps < 2000:
         t0 = time.perf_counter()
-        run_oracle(batch, nthreads=cores, conv_pool=conv_pool, ssm_pool=ssm_pool)
+        run_oracle(batch, heads=heads, nthreads=cores, conv_pool=conv_pool, ssm_pool=ssm_pool)
         el += time.perf_counter() - t0
         reps += 1
-    return {"value": reps * batch.num_actual_tokens / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"the full workload ({batch.num_actual_tokens} verify tokens, all 32 heads) repeated "
-                      f"{reps}x, {el:.1f} s of CPU time on {cores} threads"}
+    what = "all 32 v-heads" if heads is None else f"v-heads {heads[0]}..{heads[1] - 1} of {Hv}, scaled to all"
+    return {"value": reps * batch.num_actual_tokens * frac / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the full token set ({batch.num_actual_tokens} tokens), {what}, repeated {reps}x: "
+                      f"{el:.1f} s of CPU time on {cores} threads"}
+
+
+# ------------------------------------------------------------------------------------------
+# replicas: every rank runs the same workload on its own GPU; the job's time is the slowest rank
+
+def reduce_max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank floats (identity without a process group)."""
+    if dist is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch in the slowest rank's time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
 
 
 # ------------------------------------------------------------------------------------------
 
+def prefill_flops(batch) -> float:
+    """Algorithmic FLOPs of the chunked form over the prefill rows: per (64-token chunk, v-head)
+    5 c^2 d + 3 c d^2 + c^3 / 6 multiply-adds (c = 64, d = 128), two FLOPs each."""
+    c, d = 64, batch.layer.head_k_dim
+    chunks = 0
+    sub = batch.non_spec
+    qsl = sub.query_start_loc.tolist()
+    for n in range(batch.num_decodes, sub.num_seqs):
+        chunks += -(-(qsl[n + 1] - qsl[n]) // c)
+    return 2.0 * chunks * batch.layer.num_v_heads * (5 * c * c * d + 3 * c * d * d + c ** 3 / 6)
+
+
+def timed(fn, steps, flush, stream):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="spec_verify", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -170,19 +255,19 @@ def main() -> int:
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-
-    from gated_deltanet_linear_spec_gb300 import workloads
+    big = args.workload in ("mixed", "long_prefill")
+    oracle_heads = (0, 2) if big else None
 
     if args.impl == "reference":
         if rank != 0:
             return 0
-        batch = workloads.spec_verify()
-        ref = oracle_tokens_per_s(batch, budget_s=10.0)
+        batch = make_workload(args.workload)
+        ref = oracle_tokens_per_s(batch, budget_s=10.0, heads=oracle_heads)
         per_step_s = batch.num_actual_tokens / ref["value"]
         line = {"metric": METRIC, "value": ref["value"], "unit": UNIT, "n_gpus": 0, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": per_step_s * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": WORKLOAD}, "impl": "reference", "cpu_baseline": ref,
+                "config": {"workload": WORKLOADS[args.workload]}, "impl": "reference", "cpu_baseline": ref,
                 "e2e": {"value": ref["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return 0
@@ -196,108 +281,108 @@ def main() -> int:
         import torch.distributed as dist  # noqa: F811
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
-    batch = workloads.spec_verify()
+    batch = make_workload(args.workload)
     db = to_device(batch)
     alg = algorithmic_bytes(batch)
     T = batch.num_actual_tokens
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    steps = args.steps if not big else max(3, args.steps // 40)
 
-    # -------- device-timed steps (the whole path through gdn_mixed_batch)
+    # -------- device-timed steps: the whole path through gdn_mixed_batch, L2 flushed in between
     for _ in range(args.warmup):
         db.run()
         flush.zero_()
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        db.run()
-        ev[i][1].record(stream)
-        flush.zero_()
-    torch.cuda.synchronize()
+    step_ms = timed(db.run, steps, flush, stream)
     if dist:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
 
-    # -------- the recurrence kernel alone (same kernels, split into the two public calls)
-    y = torch.empty((T, batch.layer.channels), dtype=torch.float32, device="cuda")
-    rec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    conv_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    for i in range(args.steps):
-        conv_ev[i][0].record(stream)
-        gdn.gdn_conv_update(db.layer, db.params, db.pools, db.x, db.spec, y, db.status)
-        conv_ev[i][1].record(stream)
-        rec_ev[i][0].record(stream)
-        gdn.gdn_recurrent_step(db.layer, db.params, db.pools, y, db.a, db.b, db.spec, db.out, db.status)
-        rec_ev[i][1].record(stream)
-        flush.zero_()
-    torch.cuda.synchronize()
+    # -------- the dominant kernels alone, through the public entry points that launch them
+    rows = db.spec if db.spec is not None else db.non_spec
+    y = torch.empty((rows.num_tokens, batch.layer.channels), dtype=torch.float32, device="cuda")
+    conv_ms = statistics.mean(timed(lambda: gdn.gdn_conv_update(db.layer, db.params, db.pools, db.x, rows, y,
+                                                                db.status), steps, flush, stream))
+    if args.workload == "long_prefill":
+        ws = torch.empty(gdn.gdn_prefill_workspace_bytes(db.layer, rows, rows.num_seqs), dtype=torch.uint8,
+                         device="cuda")
+        kern_ms = statistics.mean(timed(lambda: gdn.gdn_chunk_prefill(db.layer, db.params, db.pools, y, db.a, db.b,
+                                                                      rows, db.out, ws, status=db.status),
+                                        steps, flush, stream))
+        peaks = measured_peaks()
+        peak = peaks.get("bf16_tflops")
+        roof = {"kernel": "gdn chunk_prep_kernel + chunk_scan_kernel (gdn_chunk_prefill)", "bound": "tensor",
+                "achieved": prefill_flops(batch) / (kern_ms * 1e-3) / 1e12, "peak": peak or FALLBACK_BF16_TFLOPS,
+                "peak_source": "measured" if peak else "fallback", "unit": "TFLOP/s", "traffic": None,
+                "algorithmic_flops_per_launch": prefill_flops(batch), "launch_ms": kern_ms, "conv_launch_ms": conv_ms}
+    else:
+        kern_ms = statistics.mean(timed(lambda: gdn.gdn_recurrent_step(db.layer, db.params, db.pools, y, db.a, db.b,
+                                                                       rows, db.out, db.status), steps, flush, stream))
+        peaks = measured_peaks()
+        peak = peaks.get("hbm_gbs")
+        src = source_hash("gdn_recurrent.cu", "gdn_internal.cuh")
+        roof = {"kernel": "gdn::recurrent_kernel", "bound": "hbm", "achieved": alg["recurrence"] / (kern_ms * 1e-3) / 1e9,
+                "peak": peak or FALLBACK_HBM_GBS, "peak_source": "measured" if peak else "fallback", "unit": "GB/s",
+                "traffic": recorded_traffic("recurrent_kernel", args.workload, src), "source_hash": src,
+                "algorithmic_bytes_per_launch": alg["recurrence"], "launch_ms": kern_ms, "conv_launch_ms": conv_ms}
+    roof["frac"] = roof["achieved"] / roof["peak"]
     clk = clocks.stop()
-    rec_ms = statistics.mean(a.elapsed_time(b) for a, b in rec_ev)
-    conv_ms = statistics.mean(a.elapsed_time(b) for a, b in conv_ev)
 
     # -------- end to end: pinned host inputs -> device -> gdn_mixed_batch -> host outputs
     host_in = {k: getattr(db, k).cpu().pin_memory() for k in ("x", "a", "b")}
-    idx_names = ("query_start_loc", "spec_state_indices", "num_accepted_tokens")
-    host_idx = {k: getattr(db.spec, k).cpu().pin_memory() for k in idx_names}
+    idx = []
+    for sub in (db.spec, db.non_spec):
+        if sub is None:
+            continue
+        for k in ("query_start_loc", "token_indx", "state_indices", "has_initial_state", "spec_state_indices",
+                  "num_accepted_tokens"):
+            t = getattr(sub, k)
+            if t is not None:
+                idx.append((t, t.cpu().pin_memory()))
     host_out = torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in list(host_in.values()) + list(host_idx.values()))
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
+        sum(h.numel() * h.element_size() for _, h in idx)
     d2h = host_out.numel() * host_out.element_size()
-    e2e_steps = max(10, args.steps // 4)
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
-    for i in range(e2e_steps):
-        e2e_ev[i][0].record(stream)
+
+    def e2e_step():
         for k, t in host_in.items():
             getattr(db, k).copy_(t, non_blocking=True)
-        for k, t in host_idx.items():
-            getattr(db.spec, k).copy_(t, non_blocking=True)
+        for dev, host in idx:
+            dev.copy_(host, non_blocking=True)
         db.run()
         host_out.copy_(db.out, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-        flush.zero_()
-    torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+
+    e2e_ms = statistics.mean(timed(e2e_step, max(3, steps // 4), flush, stream))
 
     status = int(db.status.item())
     ms = statistics.mean(step_ms)
-    if dist:
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = reduce_max_over_ranks([ms, e2e_ms], dist, device="cuda")
     if rank != 0:
         dist.destroy_process_group()
         return 0
 
-    peaks = measured_peaks()
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = peak or FALLBACK_HBM_GBS
-    achieved = alg["recurrence"] / (rec_ms * 1e-3) / 1e9
+    launches_per_step = 2 + (2 if batch.num_prefills and gdn.gdn_prefill_workspace_bytes(
+        db.layer, db.non_spec, batch.num_prefills) else 0)
     line = {
-        "metric": METRIC, "value": world * T / (ms * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": job_throughput(T, world, ms), "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "l2": "flushed between steps (512 MiB write)",
+        "config": {"workload": WORKLOADS[args.workload], "l2": "flushed between steps (512 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "hbm_gbs_whole_step": alg["total"] / (ms * 1e-3) / 1e9,
                    "algorithmic_bytes_per_step": alg["total"], "status": status},
-        "roofline": {"kernel": "gdn::recurrent_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
-                     "algorithmic_bytes_per_launch": alg["recurrence"], "launch_ms": rec_ms,
-                     "conv_launch_ms": conv_ms},
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "roofline": roof,
+        "e2e": {"value": job_throughput(T, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step * steps,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_tokens_per_s(batch)
+        line["cpu_baseline"] = oracle_tokens_per_s(batch, heads=oracle_heads)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -93,36 +93,23 @@ __global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) 
   const int n = s == 0 ? z : z - p.rows0 + p.row_off1;
   const bool reporter = (tid == 0 && blockIdx.x == 0 && h == 0);
 
+  // The prior state is the long pole: resolve its slot with as few dependent loads as possible
+  // (num_accepted -> spec_state_indices) and issue it before the row's token range is checked.
+  // Reading a valid slot is harmless even when the row turns out to be skipped.
   const int32_t bos = __ldg(R.qsl + n), eos = __ldg(R.qsl + n + 1);
-  if (bos < 0 || eos < bos || eos > R.num_tokens) {
-    if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
-    return;
-  }
-  const int L = eos - bos;
-  if (L == 0) return;
-
-  int load_slot;
+  int load_slot = 0, na = 1;
   bool read_prior;
   if (R.is_spec) {
-    if (L > R.spec_cols) {
-      if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
-      return;
-    }
-    const int na = __ldg(R.num_acc + n);
-    if (na < 1 || na > R.spec_cols) {
-      if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
-      return;
-    }
-    load_slot = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1);
+    na = __ldg(R.num_acc + n);
+    const bool na_ok = na >= 1 && na <= R.spec_cols;
+    load_slot = na_ok ? __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1) : 0;
     read_prior = load_slot > 0;
   } else {
     load_slot = __ldg(R.state_idx + n);
     read_prior = load_slot > 0 && (R.has_init == nullptr || __ldg(R.has_init + n) != 0);
   }
-  if (load_slot >= p.num_slots) {
-    if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
-    read_prior = false;
-  }
+  const bool slot_ok = load_slot < p.num_slots;
+  read_prior = read_prior && slot_ok;
 
   const int64_t head_elems = (int64_t)p.dv * DK;
   const int64_t row_off = ((int64_t)h * p.dv + dv0 + rr) * DK;  // within one slot
@@ -138,6 +125,25 @@ __global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) 
 #pragma unroll
     for (int i = 0; i < NV; ++i) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+
+  // row checks (the loads above stay in flight)
+  if (bos < 0 || eos < bos || eos > R.num_tokens) {
+    if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
+    return;
+  }
+  const int L = eos - bos;
+  if (L == 0) return;
+  if (R.is_spec) {
+    if (L > R.spec_cols) {
+      if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
+      return;
+    }
+    if (na < 1 || na > R.spec_cols) {
+      if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
+      return;
+    }
+  }
+  if (!slot_ok && reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
 
   // q|k|v may come from the conv grid launched just before (programmatic dependent launch):
   // everything above touched only the state pool and metadata; wait for that grid here.
