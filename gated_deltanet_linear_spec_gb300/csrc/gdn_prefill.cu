@@ -49,7 +49,7 @@ constexpr uint32_t kImgBytes = 90112;  // the images above: one bulk copy
 constexpr uint32_t kUt = 90112;     // U~   [t][dv]  fp32                                32 KiB
 constexpr uint32_t kMeta = 122880;  // gamma_c (fp32)
 constexpr uint32_t kScanCopy = kMeta + 16;  // what the scan kernel copies per chunk
-static_assert(kRecBytes >= kScanCopy, "record layout");
+static_assert(kRecBytes >= kScanCopy && kUt == kImgBytes, "record layout");
 
 constexpr int kPrepSmem = 81920 + 1024;
 constexpr int kScanSmem = 98304 + (int)kScanCopy + 1024;

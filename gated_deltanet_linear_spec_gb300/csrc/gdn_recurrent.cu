@@ -65,18 +65,23 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+#ifndef GDN_REC_MINB
+#define GDN_REC_MINB 8  // resident CTAs per SM the register allocation must allow
+#endif
+
 template <typename ACT, typename QT, int DK, int DVT, int LPR, int TB>
-__global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) {
+__global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const RecLaunch p) {
   constexpr int NT = DVT * LPR;
   constexpr int EPT = DK / LPR;  // fp32 state elements per thread
   constexpr int NV = EPT / 4;    // float4 words per thread
   constexpr int NWARP = NT / 32;
   constexpr int KPL = (DK + 31) / 32;  // q/k elements per lane in the norm prologue
+  constexpr int TPW = (TB + NWARP - 1) / NWARP;  // tokens each warp prepares
   static_assert(EPT % 4 == 0 && NT % 32 == 0 && (LPR & (LPR - 1)) == 0, "bad tile");
 
   __shared__ __align__(16) float sQ[TB][DK];
   __shared__ __align__(16) float sK[TB][DK];
-  __shared__ float sV[TB][DVT];
+  __shared__ __align__(16) float sV[TB][DVT];
   __shared__ float sO[TB][DVT];
   __shared__ float sEg[TB], sBeta[TB], sKQ[TB];
   __shared__ int32_t sStore[TB], sGt[TB];
@@ -127,21 +132,15 @@ __global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) 
   }
 
   // row checks (the loads above stay in flight)
-  if (bos < 0 || eos < bos || eos > R.num_tokens) {
-    if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
+  int L = eos - bos;
+  uint32_t skip = 0;
+  if (bos < 0 || eos < bos || eos > R.num_tokens) skip = GDN_STATUS_ROW_RANGE;
+  else if (L == 0) skip = 0x80000000u;
+  else if (R.is_spec && L > R.spec_cols) skip = GDN_STATUS_ROW_RANGE;
+  else if (R.is_spec && (na < 1 || na > R.spec_cols)) skip = GDN_STATUS_NUM_ACCEPTED;
+  if (skip) {
+    if (reporter && skip != 0x80000000u) set_status(p.status, skip);
     return;
-  }
-  const int L = eos - bos;
-  if (L == 0) return;
-  if (R.is_spec) {
-    if (L > R.spec_cols) {
-      if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
-      return;
-    }
-    if (na < 1 || na > R.spec_cols) {
-      if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
-      return;
-    }
   }
   if (!slot_ok && reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
 
@@ -161,17 +160,71 @@ __global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) 
     const int nt = min(TB, L - tb0);
     if (tb0) __syncthreads();  // previous batch's shared data fully consumed
 
-    // 2a. per token: L2-normalised q^ (scaled), k^, k^.q^, gates, slots -- one warp per token
-    for (int t = warp; t < nt; t += NWARP) {
-      const int64_t i = bos + tb0 + t;
-      const QT* qp = qkv + i * p.C + (int64_t)kh * DK;
-      const QT* kp = qkv + i * p.C + (int64_t)p.Hk * DK + (int64_t)kh * DK;
+    // 2a. every load of the token preparation is issued at once, so the preparation costs one
+    //     round trip: raw q and k rows and this tile's v slice land in shared memory through
+    //     cp.async (no registers held), the gate inputs and store slots through lane 0 of each
+    //     token's warp.  Warp w prepares tokens w, w+NWARP, ...
+    if constexpr (sizeof(QT) == 4 && DK % 4 == 0 && DVT % 4 == 0) {
+      constexpr int QC = DK / 4, VC = DVT / 4;  // 16-byte chunks per q/k row and per v slice
+      for (int idx = tid; idx < nt * (2 * QC + VC); idx += NT) {
+        const int t = idx / (2 * QC + VC), c = idx % (2 * QC + VC);
+        const int64_t i = bos + tb0 + t;
+        const QT* src;
+        float* dst;
+        if (c < QC) {
+          src = qkv + i * p.C + (int64_t)kh * DK + 4 * c;
+          dst = &sQ[t][4 * c];
+        } else if (c < 2 * QC) {
+          src = qkv + i * p.C + (int64_t)p.Hk * DK + (int64_t)kh * DK + 4 * (c - QC);
+          dst = &sK[t][4 * (c - QC)];
+        } else {
+          src = qkv + i * p.C + 2LL * p.Hk * DK + (int64_t)h * p.dv + dv0 + 4 * (c - 2 * QC);
+          dst = &sV[t][4 * (c - 2 * QC)];
+        }
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                     "l"(src)
+                     : "memory");
+      }
+    } else {
+      for (int idx = tid; idx < nt * (2 * DK + DVT); idx += NT) {
+        const int t = idx / (2 * DK + DVT), c = idx % (2 * DK + DVT);
+        const int64_t i = bos + tb0 + t;
+        if (c < DK) sQ[t][c] = to_f32(qkv[i * p.C + (int64_t)kh * DK + c]);
+        else if (c < 2 * DK) sK[t][c - DK] = to_f32(qkv[i * p.C + (int64_t)p.Hk * DK + (int64_t)kh * DK + c - DK]);
+        else sV[t][c - 2 * DK] = to_f32(qkv[i * p.C + 2LL * p.Hk * DK + (int64_t)h * p.dv + dv0 + c - 2 * DK]);
+      }
+    }
+    float av[TPW], bv[TPW];
+    int gt_[TPW], ss_[TPW];
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+      const int t = warp + u * NWARP;
+      av[u] = bv[u] = 0.f;
+      gt_[u] = -1;
+      ss_[u] = -1;
+      if (t < nt && lane == 0) {
+        const int gt = global_token(R, (int32_t)(bos + tb0 + t), p.num_global, p.status);
+        gt_[u] = gt;
+        if (gt >= 0) {
+          av[u] = to_f32(ga[(int64_t)gt * p.Hv + h]);
+          bv[u] = to_f32(gb[(int64_t)gt * p.Hv + h]);
+        }
+        if (R.is_spec) ss_[u] = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + tb0 + t);
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    // 2b. the arithmetic, in place: L2-normalised q^ (scaled), k^, k^.q^, gates, slots
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+      const int t = warp + u * NWARP;
+      if (t >= nt) continue;
       float qv[KPL], kv[KPL], sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int j = 0; j < KPL; ++j) {
         const int c = lane + 32 * j;
-        qv[j] = c < DK ? to_f32(qp[c]) : 0.f;
-        kv[j] = c < DK ? to_f32(kp[c]) : 0.f;
+        qv[j] = c < DK ? sQ[t][c] : 0.f;
+        kv[j] = c < DK ? sK[t][c] : 0.f;
         sq = fmaf(qv[j], qv[j], sq);
         sk = fmaf(kv[j], kv[j], sk);
       }
@@ -192,29 +245,18 @@ __global__ void __launch_bounds__(DVT* LPR) recurrent_kernel(const RecLaunch p) 
       kq = warp_sum(kq);
       if (lane == 0) {
         sKQ[t] = kq;
-        const int gt = global_token(R, (int32_t)i, p.num_global, p.status);
-        sGt[t] = gt;
-        const float av = gt >= 0 ? to_f32(ga[(int64_t)gt * p.Hv + h]) : 0.f;
-        const float bv = gt >= 0 ? to_f32(gb[(int64_t)gt * p.Hv + h]) : 0.f;
-        const float xs = av + dtb;
+        sGt[t] = gt_[u];
+        const float xs = av[u] + dtb;
         const float sp = xs > 20.f ? xs : log1pf(expf(xs));
         sEg[t] = expf(neg_A * sp);
-        sBeta[t] = 1.0f / (1.0f + expf(-bv));
-        int ss = -1;
-        if (R.is_spec) {
-          ss = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + tb0 + t);
-          if (ss >= p.num_slots) {
-            set_status(p.status, GDN_STATUS_SLOT_RANGE);
-            ss = 0;
-          }
+        sBeta[t] = 1.0f / (1.0f + expf(-bv[u]));
+        int ss = ss_[u];
+        if (ss >= p.num_slots) {
+          set_status(p.status, GDN_STATUS_SLOT_RANGE);
+          ss = 0;
         }
         sStore[t] = ss;
       }
-    }
-    // 2b. this tile's slice of v
-    for (int idx = tid; idx < nt * DVT; idx += NT) {
-      const int t = idx / DVT, r = idx % DVT;
-      sV[t][r] = to_f32(qkv[(int64_t)(bos + tb0 + t) * p.C + 2LL * p.Hk * DK + (int64_t)h * p.dv + dv0 + r]);
     }
     __syncthreads();
 
@@ -285,16 +327,21 @@ template <typename ACT, typename QT, int DK, int DVT>
 static cudaError_t launch_tile(const RecLaunch& p, int rows, bool pdl, cudaStream_t s) {
   constexpr int LPR = (DK / GDN_REC_LPR >= 4) ? GDN_REC_LPR : DK / 4;
   constexpr int TB = 8;
+  const int tiles = p.dv / DVT;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.dv / DVT, p.Hv, rows);
+  cfg.gridDim = dim3(tiles, p.Hv, rows);
   cfg.blockDim = dim3(DVT * LPR);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, recurrent_kernel<ACT, QT, DK, DVT, LPR, TB>, p);
 }
 
