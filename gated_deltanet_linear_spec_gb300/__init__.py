@@ -21,6 +21,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
 
 GDN_F32, GDN_BF16 = 0, 1
+GDN_QKV_PACKED, GDN_QKV_PER_KHEAD = 0, 1
+GDN_CONV_ROLLED, GDN_CONV_PER_SLOT = 0, 1
 STATUS_SLOT_RANGE, STATUS_NUM_ACCEPTED, STATUS_TOKEN_RANGE, STATUS_ROW_RANGE = 0x1, 0x2, 0x4, 0x8
 STATUS_WAIT_TIMEOUT = 0x10
 ERRORS = {-1: "NULL_ARG", -2: "SPEC_PAIR", -3: "SHAPE", -4: "CONSERVATION", -5: "WORKSPACE",
@@ -38,7 +40,8 @@ class _LayerDesc(ctypes.Structure):
     _fields_ = [("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
                 ("head_k_dim", ctypes.c_int32), ("head_v_dim", ctypes.c_int32),
                 ("conv_width", ctypes.c_int32), ("conv_state_len", ctypes.c_int32),
-                ("act_dtype", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("act_dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("qkv_layout", ctypes.c_int32), ("conv_layout", ctypes.c_int32)]
 
 
 class _LayerParams(ctypes.Structure):
@@ -133,6 +136,8 @@ class Layer:
     conv_state_len: int
     act_dtype: torch.dtype = torch.bfloat16
     scale: float = 0.0  # <= 0: 1/sqrt(head_k_dim)
+    qkv_layout: int = 0   # GDN_QKV_PACKED / GDN_QKV_PER_KHEAD (channel order of x)
+    conv_layout: int = 0  # GDN_CONV_ROLLED / GDN_CONV_PER_SLOT (spec conv history)
 
     @property
     def channels(self) -> int:
@@ -140,7 +145,8 @@ class Layer:
 
     def c(self) -> _LayerDesc:
         return _LayerDesc(self.num_k_heads, self.num_v_heads, self.head_k_dim, self.head_v_dim, self.conv_width,
-                          self.conv_state_len, _dtype_code(self.act_dtype), float(self.scale))
+                          self.conv_state_len, _dtype_code(self.act_dtype), float(self.scale), int(self.qkv_layout),
+                          int(self.conv_layout))
 
 
 @dataclass
@@ -262,13 +268,18 @@ def gdn_chunk_prefill(layer: Layer, params: Params, pools: Pools, qkv: torch.Ten
 def gdn_mixed_batch(layer: Layer, params: Params, pools: Pools, x: torch.Tensor, a: torch.Tensor,
                     b: torch.Tensor, non_spec: Optional[Rows], num_decodes: int, num_prefills: int,
                     spec: Optional[Rows], out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
-                    status: Optional[torch.Tensor] = None, stream=None) -> None:
+                    status: Optional[torch.Tensor] = None, stream=None,
+                    num_actual_tokens: Optional[int] = None) -> None:
+    """``num_actual_tokens`` (default x.shape[0]) may be smaller than the row count of x, a, b
+    and out, e.g. for inputs padded to a CUDA-graph bucket; rows past it are never touched."""
     act = layer.act_dtype
+    if num_actual_tokens is None:
+        num_actual_tokens = int(x.shape[0])
     if workspace is None:
         need = mixed_batch_workspace_bytes(layer, non_spec, num_prefills, spec)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     rc = library().gdn_mixed_batch(ctypes.byref(layer.c()), ctypes.byref(params.c(act)), ctypes.byref(pools.c(act)),
-                                   _ptr(x, act, "x"), _ptr(a, act, "a"), _ptr(b, act, "b"), int(x.shape[0]),
+                                   _ptr(x, act, "x"), _ptr(a, act, "a"), _ptr(b, act, "b"), int(num_actual_tokens),
                                    _rows_ref(non_spec), int(num_decodes), int(num_prefills), _rows_ref(spec),
                                    _ptr(out, act, "out"), _ptr(workspace, torch.uint8, "workspace"),
                                    workspace.numel(), _ptr(status, torch.int32, "status"), _stream(stream))

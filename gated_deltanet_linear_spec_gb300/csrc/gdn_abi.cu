@@ -35,6 +35,8 @@ int check_layer(const gdn_layer_desc* d) {
   if (d->head_v_dim <= 0 || d->head_v_dim % 16 || d->head_v_dim > 256) return GDN_ERR_SHAPE;
   if (d->conv_width < 2 || d->conv_width > 4) return GDN_ERR_SHAPE;
   if (d->conv_state_len < d->conv_width - 1) return GDN_ERR_SHAPE;
+  if (d->qkv_layout != GDN_QKV_PACKED && d->qkv_layout != GDN_QKV_PER_KHEAD) return GDN_ERR_SHAPE;
+  if (d->conv_layout != GDN_CONV_ROLLED && d->conv_layout != GDN_CONV_PER_SLOT) return GDN_ERR_SHAPE;
   return GDN_OK;
 }
 
@@ -62,7 +64,8 @@ int check_rows(const gdn_layer_desc* d, const gdn_rows* r) {
   if (has_ssi != has_na) return GDN_ERR_SPEC_PAIR;
   if (has_ssi) {
     if (r->spec_cols < 1 || r->spec_cols > kMaxSpecCols) return GDN_ERR_SHAPE;
-    if (r->spec_cols > d->conv_state_len - d->conv_width + 2) return GDN_ERR_SHAPE;
+    if (d->conv_layout == GDN_CONV_ROLLED && r->spec_cols > d->conv_state_len - d->conv_width + 2)
+      return GDN_ERR_SHAPE;
   } else if (!r->state_indices) {
     return GDN_ERR_NULL_ARG;
   }
@@ -127,6 +130,12 @@ ConvLaunch conv_args(const gdn_layer_desc* d, const gdn_layer_params* prm, const
   c.num_slots = pools->num_slots;
   c.state_len = d->conv_state_len;
   c.C = (int32_t)channels(d);
+  c.Hk = d->num_k_heads;
+  c.dk = d->head_k_dim;
+  c.Hv = d->num_v_heads;
+  c.dv = d->head_v_dim;
+  c.qkv_layout = d->qkv_layout;
+  c.conv_layout = d->conv_layout;
   c.status = status;
   return c;
 }

@@ -30,6 +30,19 @@ namespace gdn {
 // x < -88 the exponential overflows and the quotient is -0.
 __device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
+// Position in x of packed channel c: the identity for the packed layout; for the per-k-head
+// layout, k-head g's group holds q_g, k_g and the v of its Hv/Hk v-heads.  A thread's 8 channels
+// never straddle a head, so they stay contiguous in x.
+__device__ __forceinline__ int64_t x_channel(const ConvLaunch& p, int c) {
+  if (p.qkv_layout == GDN_QKV_PACKED) return c;
+  const int G = p.Hv / p.Hk, group = 2 * p.dk + G * p.dv;
+  const int qk = p.Hk * p.dk;
+  if (c < qk) return (int64_t)(c / p.dk) * group + c % p.dk;
+  if (c < 2 * qk) return (int64_t)((c - qk) / p.dk) * group + p.dk + (c - qk) % p.dk;
+  const int vc = c - 2 * qk, hv = vc / p.dv;
+  return (int64_t)(hv / G) * group + 2 * p.dk + (hv % G) * p.dv + vc % p.dv;
+}
+
 template <typename T, typename YT, int W>
 __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLaunch p) {
   asm volatile("griddepcontrol.launch_dependents;");
@@ -66,14 +79,17 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
 
   int slot, anchor;
   bool read_prior;
+  const bool per_slot = R.is_spec && p.conv_layout == GDN_CONV_PER_SLOT;
   if (R.is_spec) {
     const int na = __ldg(R.num_acc + n);
     if (na < 1 || na > R.spec_cols) {
       if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
       return;
     }
-    slot = __ldg(R.spec_idx + (int64_t)n * R.spec_cols);
-    anchor = na - 1;
+    // rolled: the history sits in column 0's slot at offset na-1; per slot: it is the snapshot
+    // taken after the last accepted token
+    slot = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + (per_slot ? na - 1 : 0));
+    anchor = per_slot ? 0 : na - 1;
     read_prior = slot > 0;
   } else {
     slot = __ldg(R.state_idx + n);
@@ -87,6 +103,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
   }
 
   const T* __restrict__ x = static_cast<const T*>(p.x);
+  const int64_t xc = x_channel(p, c0);  // where this thread's 8 channels sit in a row of x
   T* __restrict__ pool = static_cast<T*>(p.conv_pool);
   const int64_t C = p.C;
   const int64_t slot_base = (int64_t)slot * p.state_len * C + c0;
@@ -124,12 +141,12 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
       win[i] = read_prior ? load_raw8(pool + slot_base + (int64_t)(anchor + i) * C) : zero_raw8<T>();
     } else {
       const int g = global_token(R, bos + t0 - (W - 1) + i, p.num_global, p.status);
-      win[i] = g >= 0 ? load_raw8(x + (int64_t)g * C + c0) : zero_raw8<T>();
+      win[i] = g >= 0 ? load_raw8(x + (int64_t)g * C + xc) : zero_raw8<T>();
     }
   }
   // From here on this thread owns its slot elements: every read of them is done.
   const bool writer = (seg == 0 && slot > 0);
-  const bool spec_ring = writer && R.is_spec;
+  const bool spec_ring = writer && R.is_spec && !per_slot;
   if (spec_ring) {
     // spec: columns 0..W-3 <- H[1..W-2] (the shifted history); token t goes to column W-2+t below.
 #pragma unroll
@@ -144,7 +161,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
     for (int k = 0; k < G; ++k) gt[k] = (tg + k < t1) ? global_token(R, bos + tg + k, p.num_global, p.status) : -1;
     Raw8<T> xr[G];
 #pragma unroll
-    for (int k = 0; k < G; ++k) xr[k] = gt[k] >= 0 ? load_raw8(x + (int64_t)gt[k] * C + c0) : zero_raw8<T>();
+    for (int k = 0; k < G; ++k) xr[k] = gt[k] >= 0 ? load_raw8(x + (int64_t)gt[k] * C + xc) : zero_raw8<T>();
 #pragma unroll
     for (int k = 0; k < G; ++k) {
       const int t = tg + k;
@@ -166,6 +183,16 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
 #pragma unroll
       for (int i = 0; i < W - 2; ++i) win[i] = win[i + 1];
       win[W - 2] = xr[k];
+      if (per_slot) {  // the snapshot after token t goes to spec_state_indices[n, t]
+        const int ss = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + t);
+        if (ss >= p.num_slots) {
+          if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
+        } else if (ss > 0) {
+          T* dst = pool + (int64_t)ss * p.state_len * C + c0;
+#pragma unroll
+          for (int j = 0; j < W - 1; ++j) store_raw8(dst + (int64_t)j * C, win[j]);
+        }
+      }
     }
   }
 
@@ -179,7 +206,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
 #pragma unroll
       for (int j = 0; j < W - 1; ++j) {
         const int g = global_token(R, bos + L - (W - 1) + j, p.num_global, p.status);
-        store_raw8(pool + slot_base + (int64_t)j * C, g >= 0 ? load_raw8(x + (int64_t)g * C + c0) : zero_raw8<T>());
+        store_raw8(pool + slot_base + (int64_t)j * C, g >= 0 ? load_raw8(x + (int64_t)g * C + xc) : zero_raw8<T>());
       }
     }
   }

@@ -198,6 +198,9 @@ struct ConvLaunch {
   RowsDev sub[2];
   void* y[2];
   int32_t units0;  // grid.y units that belong to subset 0
+  int32_t Hk, dk, Hv, dv;
+  int32_t qkv_layout;   // gdn_qkv_layout of x
+  int32_t conv_layout;  // gdn_conv_layout of spec rows
   uint32_t* status;
 };
 

@@ -44,7 +44,7 @@ def rows_to_device(s: Optional[Subset], device) -> Optional[Rows]:
 def to_device(batch: Batch, device="cuda", pools: Optional[Pools] = None) -> DeviceBatch:
     L = batch.layer
     layer = Layer(L.num_k_heads, L.num_v_heads, L.head_k_dim, L.head_v_dim, L.conv_width, L.conv_state_len,
-                  L.act_dtype)
+                  L.act_dtype, qkv_layout=L.qkv_layout, conv_layout=L.conv_layout)
     dev = lambda t: None if t is None else t.to(device).contiguous()  # noqa: E731
     params = Params(dev(batch.conv_w), dev(batch.A_log), dev(batch.dt_bias), dev(batch.conv_b))
     if pools is None:

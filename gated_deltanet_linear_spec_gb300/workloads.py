@@ -35,10 +35,46 @@ class LayerShape:
     conv_width: int = 4
     conv_state_len: int = 3
     act_dtype: torch.dtype = torch.bfloat16
+    qkv_layout: int = 0   # 0: x packed q|k|v; 1: x per k-head groups
+    conv_layout: int = 0  # 0: rolled spec conv history at column 0; 1: one snapshot per spec slot
 
     @property
     def channels(self) -> int:
         return 2 * self.num_k_heads * self.head_k_dim + self.num_v_heads * self.head_v_dim
+
+
+def per_khead_order(layer: "LayerShape") -> torch.Tensor:
+    """Index vector P with x_per_khead[:, P[c]] = x_packed[:, c]: for each k-head g the group
+    q_g | k_g | v of the g-th block of Hv/Hk v-heads (the reorder_input=False projection order)."""
+    Hk, Hv, dk, dv = layer.num_k_heads, layer.num_v_heads, layer.head_k_dim, layer.head_v_dim
+    G = Hv // Hk
+    group = 2 * dk + G * dv
+    pos = []
+    for kind in ("q", "k"):
+        for g in range(Hk):
+            base = g * group + (0 if kind == "q" else dk)
+            pos += list(range(base, base + dk))
+    for hv in range(Hv):
+        base = (hv // G) * group + 2 * dk + (hv % G) * dv
+        pos += list(range(base, base + dv))
+    return torch.tensor(pos, dtype=torch.long)
+
+
+def with_layouts(batch: "Batch", qkv_layout: int = 0, conv_layout: int = 0) -> "Batch":
+    """The same packed-order batch seen through other layouts: with qkv_layout 1 the x columns
+    are moved to the per-k-head order; conv_layout only changes how the conv pool is read and
+    written, so the drawn pool stays as it is.  Every other tensor is shared."""
+    import copy
+    import dataclasses
+    if batch.layer.qkv_layout != 0:
+        raise ValueError("with_layouts expects a batch in the packed x order")
+    nb = copy.copy(batch)
+    nb.layer = dataclasses.replace(batch.layer, qkv_layout=qkv_layout, conv_layout=conv_layout)
+    if qkv_layout == 1:
+        x = torch.empty_like(batch.x)
+        x[:, per_khead_order(batch.layer)] = batch.x
+        nb.x = x
+    return nb
 
 
 # The layer the pages' production traffic runs (Qwen3-Next-style GDN): 16 k-heads, 32 v-heads,
@@ -310,6 +346,6 @@ def ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-__all__ = ["LayerShape", "RowSpec", "Subset", "Batch", "build_batch", "big_layer", "tiny",
+__all__ = ["LayerShape", "RowSpec", "per_khead_order", "with_layouts", "Subset", "Batch", "build_batch", "big_layer", "tiny",
            "non_spec_decode", "spec_verify", "mixed", "mixed_small", "sweep_point", "long_prefill",
            "uniform_accepts", "bytes_of", "ceil_div"]

@@ -30,8 +30,9 @@
  *   the caller owns all memory.  Calls only enqueue work on `stream` (a cudaStream_t passed as
  *   void*, NULL = legacy default stream); they never synchronise, never read device memory on
  *   the host, and allocate nothing.
- *   Dense row-major layouts, no strides.  C = 2*Hk*dk + Hv*dv packed channels ordered
- *   q (Hk*dk) | k (Hk*dk) | v (Hv*dv), head-major.  v-head h uses k-head h / (Hv/Hk).
+ *   Dense row-major layouts, no strides.  C = 2*Hk*dk + Hv*dv channels, packed as
+ *   q (Hk*dk) | k (Hk*dk) | v (Hv*dv), head-major (x may instead arrive per k-head, see
+ *   gdn_qkv_layout).  v-head h uses k-head h / (Hv/Hk).
  *   Activations (x, a, b, out, conv pool, conv weight/bias) use gdn_layer_desc.act_dtype.
  *   The SSM pool is fp32 [num_slots, Hv, dv, dk] (dk fastest).  Conv pool [num_slots,
  *   conv_state_len, C].  Slot values <= 0 are NULL: zero prior on load, no write.
@@ -77,15 +78,33 @@ typedef enum {
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
+/* Channel order of the pre-conv activation x ("[GDN] Spec-decoding-aware attention kernel",
+ * Test Plan: reorder_input).  Packed: q (Hk*dk) | k (Hk*dk) | v (Hv*dv), head-major
+ * (reorder_input=True).  Per k-head: for each k-head g, q_g (dk) | k_g (dk) | v of its
+ * G = Hv/Hk v-heads (G*dv) -- the projection order of production Qwen3-Next traffic
+ * (reorder_input=False).  Conv weights, bias, the conv pool and every post-conv tensor use the
+ * packed order in both cases. */
+typedef enum { GDN_QKV_PACKED = 0, GDN_QKV_PER_KHEAD = 1 } gdn_qkv_layout;
+
+/* How a speculative row keeps its conv history.  Rolled: one rolled history in column 0 of the
+ * row's slots, read at offset num_accepted-1 ("[GDN] Spec-decoding-aware attention kernel",
+ * Problem; needs conv_state_len >= W-2+spec_cols).  Per slot: after spec token t the last W-1
+ * inputs are written to columns 0..W-2 of spec_state_indices[n, t] and the next step reads
+ * spec_state_indices[n, num_accepted-1] ("[XE2] Support MTP of QWEN model", review thread).
+ * Non-speculative rows behave the same in both. */
+typedef enum { GDN_CONV_ROLLED = 0, GDN_CONV_PER_SLOT = 1 } gdn_conv_layout;
+
 typedef struct {
   int32_t num_k_heads;    /* Hk >= 1                                                   */
   int32_t num_v_heads;    /* Hv, a multiple of Hk                                      */
   int32_t head_k_dim;     /* dk in {16, 32, 64, 128}                                    */
   int32_t head_v_dim;     /* dv, a multiple of 16, <= 256                               */
   int32_t conv_width;     /* W in {2, 3, 4}                                             */
-  int32_t conv_state_len; /* columns per conv slot, >= W-1 (spec rows need >= W-2+spec_cols) */
+  int32_t conv_state_len; /* columns per conv slot, >= W-1 (rolled spec rows: >= W-2+spec_cols) */
   gdn_dtype act_dtype;    /* GDN_BF16 or GDN_F32                                        */
   float scale;            /* multiplies the normalised q; <= 0 selects 1/sqrt(dk)       */
+  int32_t qkv_layout;     /* gdn_qkv_layout of x                                        */
+  int32_t conv_layout;    /* gdn_conv_layout of speculative rows                        */
 } gdn_layer_desc;
 
 typedef struct {
@@ -140,13 +159,15 @@ size_t gdn_prefill_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* 
  * Conv update of one subset (step (1); "[GDN] Spec-decoding-aware attention kernel",
  * Changes, causal_conv1d.hpp bullets; the review thread of "[XE2] Support MTP of QWEN model").
  * For row n with L tokens, history h = conv_pool[slot][a : a+W-1] where
- *   spec:     slot = spec_state_indices[n, 0], a = num_accepted_tokens[n] - 1;
+ *   spec:     slot = spec_state_indices[n, 0], a = num_accepted_tokens[n] - 1 (rolled layout;
+ *             per-slot layout: slot = spec_state_indices[n, num_accepted-1], a = 0);
  *   non-spec: slot = state_indices[n], a = 0;
  * h is zero when slot <= 0 or has_initial_state[n] == 0.  With H = h ++ x[token_indx[row]]:
  *   y[t][c] = SiLU(bias[c] + sum_i conv_weight[c][i] * H[t+i][c])     (fp32 arithmetic)
  * and, after every read of the slot, the slot's columns are rewritten as bit copies:
  *   spec:     columns 0 .. W-3+L  <- H[1 .. W-2+L]   (column W-2+t holds token t)
  *   non-spec: columns 0 .. W-2    <- H[L .. L+W-2]   (the last W-1 inputs)
+ *   per-slot spec: columns 0 .. W-2 of spec_state_indices[n, t] <- H[t+1 .. t+W-1], t < L
  * other columns and slots are untouched; slot <= 0 is not written; L = 0 rows do nothing.
  *   x [num_global_tokens, C] act dtype (global order, gathered through token_indx);
  *   y [rows->num_tokens, C] in y_dtype (local order).

@@ -42,6 +42,11 @@
  *   - Spec row of L tokens (L <= spec_cols): the new history H[1 : W-1+L] goes to columns
  *     0 .. W-3+L; a non-spec row writes its last W-1 inputs H[L : L+W-1] to columns 0..W-2.
  *     Other columns stay untouched.  A row with L = 0 reads and writes nothing.
+ *   - Alternative spec conv layout (conv_layout = 1): history from column 0 of
+ *     spec_state_indices[n, num_accepted-1]; after token t the last W-1 inputs go to columns
+ *     0..W-2 of spec_state_indices[n, t].
+ *   - Alternative x layout (qkv_layout = 1): per k-head groups [q_g | k_g | v of group g];
+ *     weights, bias, the conv pool and the post-conv q|k|v stay in packed order.
  *   - Outputs are rounded to the activation type (fp32: round to nearest; bf16: round to
  *     nearest fp32 first, then round-to-nearest-even to bf16).
  */
@@ -57,6 +62,8 @@ typedef struct {
   int32_t act_is_bf16; /* 1: x, a, b, out, conv pool/weights are bf16; 0: fp32 */
   double scale;        /* multiplies q^; the caller passes 1/sqrt(dk) by default */
   double norm_eps;     /* epsilon inside the L2-norm square root */
+  int32_t qkv_layout;  /* channel order of x: 0 packed q|k|v; 1 per k-head [q_g | k_g | v of group g] */
+  int32_t conv_layout; /* spec conv state: 0 rolled history at column 0; 1 one snapshot per spec slot */
 } ref_layer;
 
 typedef struct {
@@ -137,6 +144,20 @@ static int check_row(const ref_rows* r, int32_t n, int64_t num_slots, int32_t nu
 
 /* ------------------------------------------------------------------ causal conv1d */
 
+/* Position in x of packed channel c (q | k | v blocks, head-major).  With the per-k-head
+ * layout ("[GDN] Spec-decoding-aware attention kernel", Test Plan: reorder_input=False, the
+ * projection order used in production Qwen3-Next traffic) x holds, for each k-head g in turn,
+ * q_g (dk), k_g (dk) and the dv-channel v of the G = Hv/Hk v-heads of group g. */
+static int64_t x_channel(const ref_layer* L, int64_t c) {
+  if (!L->qkv_layout) return c;
+  const int64_t dk = L->head_k_dim, dv = L->head_v_dim, Hk = L->num_k_heads, G = L->num_v_heads / Hk;
+  const int64_t group = 2 * dk + G * dv;
+  if (c < Hk * dk) return (c / dk) * group + c % dk;                    /* q of k-head c/dk */
+  if (c < 2 * Hk * dk) return ((c - Hk * dk) / dk) * group + dk + c % dk; /* k */
+  const int64_t vc = c - 2 * Hk * dk, hv = vc / dv;                     /* v of v-head hv */
+  return (hv / G) * group + 2 * dk + (hv % G) * dv + vc % dv;
+}
+
 /*
  * Conv update of one subset.  conv_pool [P, state_len, C] (act type) is read and written;
  * y [num_tokens, C] (double, local token order) receives SiLU(conv).
@@ -153,7 +174,14 @@ int gdn_ref_conv(const ref_layer* L, const void* conv_w, const void* conv_b, voi
     const int32_t bos = rows->query_start_loc[n], len = rows->query_start_loc[n + 1] - bos;
     if (len == 0) continue;
     int32_t slot, anchor, read_prior;
-    if (rows->is_spec) {
+    const int per_slot = rows->is_spec && L->conv_layout == 1;
+    if (per_slot) {
+      /* one snapshot per spec slot ("[XE2] Support MTP of QWEN model", review thread): the
+       * history is the snapshot taken after the last accepted token */
+      slot = rows->spec_state_indices[(int64_t)n * rows->spec_cols + rows->num_accepted_tokens[n] - 1];
+      anchor = 0;
+      read_prior = slot > 0;
+    } else if (rows->is_spec) {
       slot = rows->spec_state_indices[(int64_t)n * rows->spec_cols]; /* column 0 of the row */
       anchor = rows->num_accepted_tokens[n] - 1;
       read_prior = slot > 0;
@@ -182,8 +210,8 @@ int gdn_ref_conv(const ref_layer* L, const void* conv_w, const void* conv_b, voi
     for (int32_t t = 0; t < len; ++t) {
       int64_t gt = global_token(rows, bos + t);
       for (int64_t c = 0; c < C; ++c) {
-        H[(W - 1 + t) * C + c] = act_get(x, gt * C + c, bf);
-        act_copy(Hraw, (W - 1 + t) * C + c, x, gt * C + c, bf);
+        H[(W - 1 + t) * C + c] = act_get(x, gt * C + x_channel(L, c), bf);
+        act_copy(Hraw, (W - 1 + t) * C + c, x, gt * C + x_channel(L, c), bf);
       }
     }
     /* y_t[c] = SiLU(bias[c] + sum_i w[c][i] * H[t+i][c]) */
@@ -193,8 +221,18 @@ int gdn_ref_conv(const ref_layer* L, const void* conv_w, const void* conv_b, voi
         for (int32_t i = 0; i < W; ++i) acc += act_get(conv_w, c * W + i, bf) * H[(t + i) * C + c];
         y[(int64_t)(bos + t) * C + c] = silu(acc);
       }
-    /* Rolled history back into the slot, after every read of it. */
-    if (slot > 0) {
+    /* Per-slot snapshots: after token t, its last W-1 inputs H[t+1 .. t+W-1] go to
+     * spec_state_indices[n, t] (slots <= 0 skipped). */
+    if (per_slot) {
+      for (int32_t t = 0; t < len; ++t) {
+        const int32_t ss = rows->spec_state_indices[(int64_t)n * rows->spec_cols + t];
+        if (ss <= 0) continue;
+        for (int32_t j = 0; j < W - 1; ++j)
+          for (int64_t c = 0; c < C; ++c)
+            act_copy(conv_pool, ((int64_t)ss * SL + j) * C + c, Hraw, (int64_t)(t + 1 + j) * C + c, bf);
+      }
+    } else if (slot > 0) {
+      /* Rolled history back into the slot, after every read of it. */
       int32_t off = rows->is_spec ? 1 : len;
       int32_t ncols = rows->is_spec ? W - 2 + len : W - 1;
       for (int32_t j = 0; j < ncols; ++j)

@@ -43,7 +43,7 @@ class _Layer(ctypes.Structure):
                 ("head_k_dim", ctypes.c_int32), ("head_v_dim", ctypes.c_int32),
                 ("conv_width", ctypes.c_int32), ("conv_state_len", ctypes.c_int32),
                 ("act_is_bf16", ctypes.c_int32), ("scale", ctypes.c_double),
-                ("norm_eps", ctypes.c_double)]
+                ("norm_eps", ctypes.c_double), ("qkv_layout", ctypes.c_int32), ("conv_layout", ctypes.c_int32)]
 
 
 class _Rows(ctypes.Structure):
@@ -84,6 +84,8 @@ class Layer:
     act_bf16: bool = True
     scale: Optional[float] = None  # None -> 1/sqrt(head_k_dim)
     norm_eps: float = 1e-6
+    qkv_layout: int = 0   # 0 packed q|k|v; 1 per k-head groups (x only)
+    conv_layout: int = 0  # 0 rolled history at column 0; 1 one snapshot per spec slot
 
     @property
     def channels(self) -> int:
@@ -93,7 +95,7 @@ class Layer:
         scale = self.scale if self.scale is not None else 1.0 / np.sqrt(self.head_k_dim)
         return _Layer(self.num_k_heads, self.num_v_heads, self.head_k_dim, self.head_v_dim,
                       self.conv_width, self.conv_state_len, int(self.act_bf16), float(scale),
-                      float(self.norm_eps))
+                      float(self.norm_eps), int(self.qkv_layout), int(self.conv_layout))
 
 
 @dataclass

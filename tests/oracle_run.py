@@ -34,7 +34,8 @@ def act_to_f64(a: np.ndarray) -> np.ndarray:
 def oracle_layer(batch: Batch, scale: Optional[float] = None) -> oracle.Layer:
     L = batch.layer
     return oracle.Layer(L.num_k_heads, L.num_v_heads, L.head_k_dim, L.head_v_dim, L.conv_width,
-                        L.conv_state_len, L.act_dtype == torch.bfloat16, scale)
+                        L.conv_state_len, L.act_dtype == torch.bfloat16, scale,
+                        qkv_layout=L.qkv_layout, conv_layout=L.conv_layout)
 
 
 def oracle_rows(s: Optional[Subset]) -> Optional[oracle.Rows]:

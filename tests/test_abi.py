@@ -44,7 +44,7 @@ def test_every_declared_function_is_exported(lib):
 
 def big_layer(**kw):
     d = dict(num_k_heads=16, num_v_heads=32, head_k_dim=128, head_v_dim=128, conv_width=4, conv_state_len=6,
-             act_dtype=gdn.GDN_BF16, scale=0.0)
+             act_dtype=gdn.GDN_BF16, scale=0.0, qkv_layout=0, conv_layout=0)
     d.update(kw)
     return _LayerDesc(**d)
 
@@ -118,14 +118,18 @@ def test_spec_pair_is_required(lib):
 
 
 @pytest.mark.parametrize("kw", [dict(num_v_heads=24), dict(head_k_dim=48), dict(head_v_dim=72),
-                                dict(conv_width=5), dict(conv_state_len=2), dict(num_k_heads=0)])
+                                dict(conv_width=5), dict(conv_state_len=2), dict(num_k_heads=0),
+                                dict(qkv_layout=2), dict(conv_layout=3)])
 def test_shape_checks(lib, kw):
     assert mixed(lib, layer=big_layer(**kw)) == ERR["SHAPE"]
 
 
 def test_spec_cols_must_fit_the_conv_ring(lib):
-    # state_len 6 with W = 4 holds at most 4 verify tokens per row
+    # state_len 6 with W = 4 holds at most 4 verify tokens per row in the rolled layout
     assert mixed(lib, spec=spec_rows(k=5, token_indx=FAKE)) == ERR["SHAPE"]
+    # the per-slot layout keeps W-1 columns per slot, so the same row only reaches the workspace check
+    assert mixed(lib, spec=spec_rows(k=5, token_indx=FAKE), layer=big_layer(conv_layout=1),
+                 ws_bytes=16) == ERR["WORKSPACE"]
     assert mixed(lib, spec=spec_rows(k=65, token_indx=FAKE), layer=big_layer(conv_state_len=80)) == ERR["SHAPE"]
 
 
