@@ -109,15 +109,20 @@ def algorithmic_bytes(batch) -> dict:
                 na = int(sub.num_accepted_tokens[n])
                 loads += ssi[na - 1] > 0
                 stores += sum(1 for t in range(ln) if ssi[t] > 0)
-                if ssi[0] > 0:
+                if L.conv_layout == 1:  # one W-1 snapshot read, one written per non-NULL verify slot
+                    conv += ((W - 1) * (ssi[na - 1] > 0) + (W - 1) * sum(ssi[t] > 0 for t in range(ln))) * C * act
+                elif ssi[0] > 0:
                     conv += (W - 1 + W - 2 + ln) * C * act
             else:
                 s = int(sub.state_indices[n])
                 hi = 1 if sub.has_initial_state is None else int(sub.has_initial_state[n])
-                loads += (s > 0 and hi != 0)
+                src = s
+                if sub.num_accepted_tokens is not None:  # acceptance-aware rows load the accepted state
+                    src = int(sub.spec_state_indices[n, int(sub.num_accepted_tokens[n]) - 1])
+                loads += (src > 0 and hi != 0)
                 stores += s > 0
-                if s > 0:
-                    conv += ((W - 1) * (hi != 0) + (W - 1)) * C * act
+                conv_src = src if (sub.num_accepted_tokens is not None and L.conv_layout == 1) else s
+                conv += ((W - 1) * (conv_src > 0 and hi != 0) + (W - 1) * (s > 0)) * C * act
     T = batch.num_actual_tokens
     ssm = (loads + stores) * state
     io = T * (C * act + 2 * Hv * act + Hv * dv * act)
@@ -249,6 +254,11 @@ def main() -> int:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="spec_verify", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--qkv-layout", default="packed", choices=["packed", "per_khead"],
+                    help="channel order of x (per_khead: the reorder_input=False projection order)")
+    ap.add_argument("--conv-layout", default="rolled", choices=["rolled", "per_slot"],
+                    help="spec conv history: rolled at column 0, or one snapshot per spec slot")
+    ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of the step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -281,7 +291,9 @@ def main() -> int:
         import torch.distributed as dist  # noqa: F811
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
-    batch = make_workload(args.workload)
+    from gated_deltanet_linear_spec_gb300.workloads import with_layouts
+    batch = with_layouts(make_workload(args.workload), qkv_layout=int(args.qkv_layout == "per_khead"),
+                         conv_layout=int(args.conv_layout == "per_slot"))
     db = to_device(batch)
     alg = algorithmic_bytes(batch)
     T = batch.num_actual_tokens
@@ -294,11 +306,21 @@ def main() -> int:
         db.run()
         flush.zero_()
     torch.cuda.synchronize()
+    step_fn = db.run
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            db.run()
+        for _ in range(args.warmup):
+            graph.replay()
+            flush.zero_()
+        torch.cuda.synchronize()
+        step_fn = graph.replay
     clocks = ClockSampler(local_rank)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    step_ms = timed(db.run, steps, flush, stream)
+    step_ms = timed(step_fn, steps, flush, stream)
     if dist:
         dist.barrier()
 
@@ -373,6 +395,8 @@ def main() -> int:
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "l2": "flushed between steps (512 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
+                   "qkv_layout": args.qkv_layout, "conv_layout": args.conv_layout,
+                   "launch": "cuda graph replay" if args.graph else "eager",
                    "hbm_gbs_whole_step": alg["total"] / (ms * 1e-3) / 1e9,
                    "algorithmic_bytes_per_step": alg["total"], "status": status},
         "roofline": roof,

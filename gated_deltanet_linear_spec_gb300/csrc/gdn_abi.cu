@@ -72,7 +72,9 @@ int check_rows(const gdn_layer_desc* d, const gdn_rows* r) {
   return GDN_OK;
 }
 
-bool is_spec(const gdn_rows* r) { return r && r->spec_state_indices != nullptr; }
+// Spec rows have spec slots and no state_indices; a non-spec subset may carry the spec pair
+// as the acceptance of its rows' previous verify step.
+bool is_spec(const gdn_rows* r) { return r && r->spec_state_indices != nullptr && r->state_indices == nullptr; }
 int nseq(const gdn_rows* r) { return r ? r->num_seqs : 0; }
 int ntok(const gdn_rows* r) { return r ? r->num_tokens : 0; }
 

@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
   if (t0 >= L) return;
   const int t1 = min(L, t0 + kConvSeg);
 
-  int slot, anchor;
+  int slot, anchor;  // the row's conv slot; the history's column offset
+  int rd;            // the slot the history is read from
   bool read_prior;
   const bool per_slot = R.is_spec && p.conv_layout == GDN_CONV_PER_SLOT;
   if (R.is_spec) {
@@ -88,17 +89,27 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
     }
     // rolled: the history sits in column 0's slot at offset na-1; per slot: it is the snapshot
     // taken after the last accepted token
-    slot = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + (per_slot ? na - 1 : 0));
+    slot = rd = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + (per_slot ? na - 1 : 0));
     anchor = per_slot ? 0 : na - 1;
-    read_prior = slot > 0;
+    read_prior = rd > 0;
   } else {
-    slot = __ldg(R.state_idx + n);
+    slot = rd = __ldg(R.state_idx + n);
     anchor = 0;
-    read_prior = slot > 0 && (R.has_init == nullptr || __ldg(R.has_init + n) != 0);
+    if (R.num_acc) {
+      // acceptance-aware row: the history its previous verify step accepted
+      const int na = __ldg(R.num_acc + n);
+      if (na < 1 || na > R.spec_cols) {
+        if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
+        return;
+      }
+      if (p.conv_layout == GDN_CONV_PER_SLOT) rd = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1);
+      else anchor = na - 1;
+    }
+    read_prior = rd > 0 && (R.has_init == nullptr || __ldg(R.has_init + n) != 0);
   }
-  if (slot >= p.num_slots) {
+  if (slot >= p.num_slots || rd >= p.num_slots) {
     if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
-    slot = 0;
+    if (slot >= p.num_slots) slot = 0;
     read_prior = false;
   }
 
@@ -107,6 +118,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
   T* __restrict__ pool = static_cast<T*>(p.conv_pool);
   const int64_t C = p.C;
   const int64_t slot_base = (int64_t)slot * p.state_len * C + c0;
+  const int64_t hist_base = (int64_t)(read_prior ? rd : 0) * p.state_len * C + c0;
 
   // Weights and bias of the thread's 8 channels: 8*W contiguous elements, 16-byte vectors.
   float w[W][8], bias[8];
@@ -138,7 +150,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
 #pragma unroll
   for (int i = 0; i < W - 1; ++i) {
     if (seg == 0) {
-      win[i] = read_prior ? load_raw8(pool + slot_base + (int64_t)(anchor + i) * C) : zero_raw8<T>();
+      win[i] = read_prior ? load_raw8(pool + hist_base + (int64_t)(anchor + i) * C) : zero_raw8<T>();
     } else {
       const int g = global_token(R, bos + t0 - (W - 1) + i, p.num_global, p.status);
       win[i] = g >= 0 ? load_raw8(x + (int64_t)g * C + xc) : zero_raw8<T>();

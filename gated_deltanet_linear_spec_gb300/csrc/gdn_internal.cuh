@@ -15,13 +15,22 @@ struct RowsDev {
   const int32_t* tok;        // NULL = identity
   const int32_t* state_idx;  // non-spec
   const int32_t* has_init;   // non-spec, NULL = all 1
-  const int32_t* spec_idx;   // spec [num_seqs, spec_cols]
-  const int32_t* num_acc;    // spec
+  const int32_t* spec_idx;   // spec [num_seqs, spec_cols]; acceptance-aware non-spec rows too
+  const int32_t* num_acc;    // spec; acceptance-aware non-spec rows too (else NULL)
   int32_t spec_cols;
   int32_t num_seqs;
   int32_t num_tokens;
   int32_t is_spec;
 };
+
+// Slot of a non-spec row's prior SSM state: state_indices[n], or for acceptance-aware rows
+// the previous verify step's slot of its last accepted token.  -1: num_accepted out of range.
+__device__ __forceinline__ int32_t non_spec_load_slot(const RowsDev& R, int n) {
+  if (R.num_acc == nullptr) return __ldg(R.state_idx + n);
+  const int na = __ldg(R.num_acc + n);
+  if (na < 1 || na > R.spec_cols) return -1;
+  return __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1);
+}
 
 __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bit) {
   if (st) atomicOr(st, bit);
@@ -178,7 +187,7 @@ inline RowsDev rows_dev(const gdn_rows* r) {
   d.spec_cols = r->spec_cols;
   d.num_seqs = r->num_seqs;
   d.num_tokens = r->num_tokens;
-  d.is_spec = (r->spec_state_indices != nullptr) ? 1 : 0;
+  d.is_spec = (r->spec_state_indices != nullptr && r->state_indices == nullptr) ? 1 : 0;
   return d;
 }
 

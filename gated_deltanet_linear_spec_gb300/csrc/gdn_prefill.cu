@@ -402,14 +402,20 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   const int L = eos - bos;
   const int nch = (L + kCh - 1) / kCh;
   int slot = __ldg(p.rows.state_idx + n);
-  bool read_prior = slot > 0 && (p.rows.has_init == nullptr || __ldg(p.rows.has_init + n) != 0);
-  if (slot >= p.num_slots) {
+  const int load_slot = non_spec_load_slot(p.rows, n);
+  if (load_slot < 0) {  // acceptance-aware row with num_accepted out of range
+    if (tid == 0 && h == 0) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
+    return;
+  }
+  bool read_prior = load_slot > 0 && (p.rows.has_init == nullptr || __ldg(p.rows.has_init + n) != 0);
+  if (slot >= p.num_slots || load_slot >= p.num_slots) {
     if (tid == 0 && h == 0) set_status(p.status, GDN_STATUS_SLOT_RANGE);
-    slot = 0;
+    if (slot >= p.num_slots) slot = 0;
     read_prior = false;
   }
   const int d = 32 * warp + lane;
   float* gS = p.ssm_pool + ((int64_t)slot * p.Hv + h) * kD * kD + (int64_t)d * kD;
+  const float* gS0 = p.ssm_pool + ((int64_t)(read_prior ? load_slot : 0) * p.Hv + h) * kD * kD + (int64_t)d * kD;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 
   if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
@@ -429,7 +435,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
-      float4 f = read_prior ? *reinterpret_cast<const float4*>(gS + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 f = read_prior ? *reinterpret_cast<const float4*>(gS0 + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       v[j] = f.x; v[j + 1] = f.y; v[j + 2] = f.z; v[j + 3] = f.w;
     }
     tc::tmem_st32(tc::tmem_lane_col(tS, warp, c0), v);

@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
     load_slot = na_ok ? __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1) : 0;
     read_prior = load_slot > 0;
   } else {
-    load_slot = __ldg(R.state_idx + n);
+    load_slot = non_spec_load_slot(R, n);
+    if (load_slot < 0) na = 0;  // acceptance out of range: flagged below
     read_prior = load_slot > 0 && (R.has_init == nullptr || __ldg(R.has_init + n) != 0);
   }
   const bool slot_ok = load_slot < p.num_slots;
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   if (bos < 0 || eos < bos || eos > R.num_tokens) skip = GDN_STATUS_ROW_RANGE;
   else if (L == 0) skip = 0x80000000u;
   else if (R.is_spec && L > R.spec_cols) skip = GDN_STATUS_ROW_RANGE;
-  else if (R.is_spec && (na < 1 || na > R.spec_cols)) skip = GDN_STATUS_NUM_ACCEPTED;
+  else if ((R.is_spec || R.num_acc) && (na < 1 || na > R.spec_cols)) skip = GDN_STATUS_NUM_ACCEPTED;
   if (skip) {
     if (reporter && skip != 0x80000000u) set_status(p.status, skip);
     return;

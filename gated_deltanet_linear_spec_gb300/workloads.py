@@ -87,8 +87,9 @@ def big_layer(state_len: int, act_dtype: torch.dtype = torch.bfloat16) -> LayerS
 class RowSpec:
     kind: str                      # "spec" | "decode" | "prefill"
     length: int
-    num_accepted: int = 1          # spec rows: accepted tokens of the previous step, 1..spec_cols
+    num_accepted: int = 1          # spec and aware rows: accepted tokens of the previous step, 1..spec_cols
     has_initial_state: bool = True  # non-spec rows
+    aware: bool = False            # non-spec rows: carries its previous verify step's acceptance
 
 
 @dataclass
@@ -103,7 +104,8 @@ class Subset:
 
     @property
     def is_spec(self) -> bool:
-        return self.spec_state_indices is not None
+        # a non-spec subset may carry spec_state_indices too (acceptance-aware rows)
+        return self.spec_state_indices is not None and self.state_indices is None
 
     @property
     def num_seqs(self) -> int:
@@ -210,7 +212,11 @@ def build_batch(layer: LayerShape, rows: List[RowSpec], *, num_slots: int, spec_
     pre_ids = sorted([i for i, r in enumerate(rows) if r.kind == "prefill"], key=lambda i: row_start[i])
     ns_ids = dec_ids + pre_ids
 
-    need = len(spec_ids) * spec_cols + len(ns_ids)
+    aware = any(rows[i].aware for i in ns_ids)
+    if aware and spec_cols < 1:
+        raise ValueError("acceptance-aware rows need spec_cols >= 1")
+    base_need = len(spec_ids) * spec_cols + len(ns_ids)
+    need = base_need + (len(ns_ids) * (spec_cols - 1) if aware else 0)
     if need > num_slots - 1:
         raise ValueError(f"pool of {num_slots} slots cannot give {need} distinct non-NULL slots")
     slots = (torch.randperm(num_slots - 1, generator=gen)[:need] + 1).to(torch.int32)
@@ -238,11 +244,18 @@ def build_batch(layer: LayerShape, rows: List[RowSpec], *, num_slots: int, spec_
         spec = Subset(qsl, tok, spec_state_indices=ssi, num_accepted_tokens=na)
     if ns_ids:
         qsl, tok = subset(ns_ids, False)
-        si = slots[len(spec_ids) * spec_cols: need].clone()
+        si = slots[len(spec_ids) * spec_cols: base_need].clone()
         for rr in (non_spec_nulls or []):
             si[rr] = 0
         hi = torch.tensor([int(rows[i].has_initial_state) for i in ns_ids], dtype=torch.int32)
         non_spec = Subset(qsl, tok, state_indices=si, has_initial_state=hi)
+        if aware:
+            # the previous verify step's slots: column 0 is the row's own slot (a block table
+            # row), the others fresh; rows that are not aware accepted exactly one token
+            ssi = torch.cat([si[:, None], slots[base_need:need].reshape(len(ns_ids), spec_cols - 1)], 1)
+            non_spec.spec_state_indices = ssi.contiguous()
+            non_spec.num_accepted_tokens = torch.tensor(
+                [rows[i].num_accepted if rows[i].aware else 1 for i in ns_ids], dtype=torch.int32)
 
     # token_indx is only passed when it is not the identity (or when asked for).
     for s in (spec, non_spec):

@@ -121,8 +121,17 @@ typedef struct {
 } gdn_pools;
 
 /*
- * One subset of rows.  A subset is speculative when spec_state_indices and
- * num_accepted_tokens are given (both, or GDN_ERR_SPEC_PAIR), otherwise non-speculative.
+ * One subset of rows.  spec_state_indices and num_accepted_tokens come as a pair (both, or
+ * GDN_ERR_SPEC_PAIR).  A subset is speculative when it has the pair and no state_indices.
+ * A non-speculative subset (state_indices given) may also carry the pair: its rows are then
+ * acceptance-aware, i.e. each continues from what its previous verify step accepted -- a
+ * verify row cut to a prefix by the batch token budget and scheduled as a plain row ("[Bugfix]
+ * Align Qwen GDN gates with speculative tokens", the second mechanism in the reachability
+ * comment).  Such a row reads its conv history at column offset num_accepted-1 of
+ * state_indices[n] (rolled layout) or from spec_state_indices[n, num_accepted-1] (per-slot
+ * layout), loads its SSM state from spec_state_indices[n, num_accepted-1], and writes like any
+ * non-spec row.  A row that accepted one token with spec_state_indices[n, 0] == state_indices[n]
+ * is an ordinary non-spec row.
  * Local tokens are numbered 0..num_tokens-1 in row order; row n owns local tokens
  * [query_start_loc[n], query_start_loc[n+1]).
  */
@@ -133,8 +142,10 @@ typedef struct {
   const int32_t* token_indx;          /* [T_sub] global token of each local token; NULL = identity */
   const int32_t* state_indices;       /* non-spec: [N_sub] conv+SSM slot of each row              */
   const int32_t* has_initial_state;   /* non-spec: [N_sub], 0 = start from zeros; NULL = all 1    */
-  const int32_t* spec_state_indices;  /* spec: [N_sub, spec_cols]; column 0 is also the conv slot */
-  const int32_t* num_accepted_tokens; /* spec: [N_sub], in [1, spec_cols]                          */
+  const int32_t* spec_state_indices;  /* spec: [N_sub, spec_cols]; column 0 is also the conv slot;
+                                         non-spec: the previous verify step's slots, or NULL     */
+  const int32_t* num_accepted_tokens; /* spec (and acceptance-aware non-spec): [N_sub], in
+                                         [1, spec_cols]                                          */
   int32_t spec_cols;                  /* spec: columns of spec_state_indices, 1..64                */
 } gdn_rows;
 
@@ -161,8 +172,9 @@ size_t gdn_prefill_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* 
  * For row n with L tokens, history h = conv_pool[slot][a : a+W-1] where
  *   spec:     slot = spec_state_indices[n, 0], a = num_accepted_tokens[n] - 1 (rolled layout;
  *             per-slot layout: slot = spec_state_indices[n, num_accepted-1], a = 0);
- *   non-spec: slot = state_indices[n], a = 0;
- * h is zero when slot <= 0 or has_initial_state[n] == 0.  With H = h ++ x[token_indx[row]]:
+ *   non-spec: slot = state_indices[n], a = 0 (acceptance-aware rows: a = num_accepted-1, or
+ *             with the per-slot layout the history slot spec_state_indices[n, num_accepted-1]);
+ * h is zero when the history slot is <= 0 or has_initial_state[n] == 0.  With H = h ++ x[token_indx[row]]:
  *   y[t][c] = SiLU(bias[c] + sum_i conv_weight[c][i] * H[t+i][c])     (fp32 arithmetic)
  * and, after every read of the slot, the slot's columns are rewritten as bit copies:
  *   spec:     columns 0 .. W-3+L  <- H[1 .. W-2+L]   (column W-2+t holds token t)
@@ -179,8 +191,9 @@ int gdn_conv_update(const gdn_layer_desc* layer, const gdn_layer_params* params,
 /*
  * Gated delta rule over one subset, token by token (step (2); "[GDN] Spec-decoding-aware
  * attention kernel", Changes, gated_delta_rule.hpp bullet).  For v-head h of row n:
- *   load S (dv x dk) from spec_state_indices[n, num_accepted[n]-1] (spec) or state_indices[n]
- *   (non-spec; zeros when has_initial_state[n] == 0); zeros when the slot is <= 0;
+ *   load S (dv x dk) from spec_state_indices[n, num_accepted[n]-1] (spec, and acceptance-aware
+ *   non-spec rows) or state_indices[n] (other non-spec rows); zeros for a non-spec row with
+ *   has_initial_state[n] == 0 and whenever the slot is <= 0;
  *   per token: g = -exp(A_log[h]) softplus(a + dt_bias[h]) (softplus(x) = x for x > 20),
  *   beta = sigmoid(b), q^ = q / sqrt(|q|^2 + 1e-6) * scale, k^ = k / sqrt(|k|^2 + 1e-6),
  *   S <- e^g S (I - beta k^ k^T) + beta v k^T,  out[token_indx[i]][h] = S q^;

@@ -47,6 +47,8 @@
  *     0..W-2 of spec_state_indices[n, t].
  *   - Alternative x layout (qkv_layout = 1): per k-head groups [q_g | k_g | v of group g];
  *     weights, bias, the conv pool and the post-conv q|k|v stay in packed order.
+ *   - A non-spec row given num_accepted_tokens and spec_state_indices continues from its
+ *     previous verify step's accepted state (see acceptance_aware below).
  *   - Outputs are rounded to the activation type (fp32: round to nearest; bf16: round to
  *     nearest fp32 first, then round-to-nearest-even to bf16).
  */
@@ -74,6 +76,8 @@ typedef struct {
   const int32_t* has_initial_state;   /* non-spec rows: [num_seqs] or NULL (= all 1) */
   const int32_t* spec_state_indices;  /* spec rows: [num_seqs, spec_cols] */
   const int32_t* num_accepted_tokens; /* spec rows: [num_seqs] */
+  /* Non-spec rows may carry spec_state_indices and num_accepted_tokens too: the slots and the
+   * acceptance of the row's previous verify step (acceptance-aware rows, below). */
   int32_t spec_cols;
   int32_t is_spec;
 } ref_rows;
@@ -138,9 +142,24 @@ static int check_row(const ref_rows* r, int32_t n, int64_t num_slots, int32_t nu
       if (r->spec_state_indices[(int64_t)n * r->spec_cols + j] >= num_slots) return -1;
   } else {
     if (r->state_indices[n] >= num_slots) return -1;
+    if (r->num_accepted_tokens) {
+      int32_t na = r->num_accepted_tokens[n];
+      if (eos > bos && (na < 1 || na > r->spec_cols)) return -1;
+      for (int32_t j = 0; j < r->spec_cols; ++j)
+        if (r->spec_state_indices[(int64_t)n * r->spec_cols + j] >= num_slots) return -1;
+    }
   }
   return 0;
 }
+
+/* A non-spec row that carries its previous verify step's acceptance: a verify row cut to a
+ * prefix by the batch budget and scheduled as a plain row ("[Bugfix] Align Qwen GDN gates with
+ * speculative tokens", the second mechanism in the reachability comment).  Its history and
+ * prior state are where that step's accepted tokens left them: conv history at column
+ * offset num_accepted-1 of state_indices[n] (rolled layout) or in the snapshot slot
+ * spec_state_indices[n, num_accepted-1] (per-slot layout); SSM state from
+ * spec_state_indices[n, num_accepted-1].  Writes are those of any non-spec row. */
+static int acceptance_aware(const ref_rows* r) { return !r->is_spec && r->num_accepted_tokens != NULL; }
 
 /* ------------------------------------------------------------------ causal conv1d */
 
@@ -173,22 +192,29 @@ int gdn_ref_conv(const ref_layer* L, const void* conv_w, const void* conv_b, voi
   for (int32_t n = 0; n < rows->num_seqs; ++n) {
     const int32_t bos = rows->query_start_loc[n], len = rows->query_start_loc[n + 1] - bos;
     if (len == 0) continue;
-    int32_t slot, anchor, read_prior;
+    /* slot: the row's own conv slot (read and rolled back); rd: where the history is read */
+    int32_t slot, rd, anchor, read_prior;
     const int per_slot = rows->is_spec && L->conv_layout == 1;
+    const int aware = acceptance_aware(rows);
     if (per_slot) {
       /* one snapshot per spec slot ("[XE2] Support MTP of QWEN model", review thread): the
        * history is the snapshot taken after the last accepted token */
-      slot = rows->spec_state_indices[(int64_t)n * rows->spec_cols + rows->num_accepted_tokens[n] - 1];
+      slot = rd = rows->spec_state_indices[(int64_t)n * rows->spec_cols + rows->num_accepted_tokens[n] - 1];
       anchor = 0;
-      read_prior = slot > 0;
+      read_prior = rd > 0;
     } else if (rows->is_spec) {
-      slot = rows->spec_state_indices[(int64_t)n * rows->spec_cols]; /* column 0 of the row */
+      slot = rd = rows->spec_state_indices[(int64_t)n * rows->spec_cols]; /* column 0 of the row */
       anchor = rows->num_accepted_tokens[n] - 1;
-      read_prior = slot > 0;
+      read_prior = rd > 0;
     } else {
-      slot = rows->state_indices[n];
+      slot = rd = rows->state_indices[n];
       anchor = 0;
-      read_prior = slot > 0 && (rows->has_initial_state ? rows->has_initial_state[n] != 0 : 1);
+      if (aware) {
+        const int32_t a = rows->num_accepted_tokens[n] - 1;
+        if (L->conv_layout == 1) rd = rows->spec_state_indices[(int64_t)n * rows->spec_cols + a];
+        else anchor = a;
+      }
+      read_prior = rd > 0 && (rows->has_initial_state ? rows->has_initial_state[n] != 0 : 1);
     }
     /* H = (W-1 history columns) ++ (the row's len inputs), kept both as exact values and as
      * the raw stored elements so that the slot write is a bit copy. */
@@ -199,7 +225,7 @@ int gdn_ref_conv(const ref_layer* L, const void* conv_w, const void* conv_b, voi
     for (int32_t i = 0; i < W - 1; ++i)
       for (int64_t c = 0; c < C; ++c) {
         if (read_prior) {
-          int64_t src = ((int64_t)slot * SL + anchor + i) * C + c;
+          int64_t src = ((int64_t)rd * SL + anchor + i) * C + c;
           H[i * C + c] = act_get(conv_pool, src, bf);
           act_copy(Hraw, i * C + c, conv_pool, src, bf);
         } else {
@@ -277,7 +303,9 @@ static void recurrent_row_head(const rec_job* J, int32_t n, int32_t h) {
     load_slot = r->spec_state_indices[(int64_t)n * r->spec_cols + r->num_accepted_tokens[n] - 1];
     read_prior = load_slot > 0;
   } else {
-    load_slot = r->state_indices[n];
+    load_slot = acceptance_aware(r)
+                    ? r->spec_state_indices[(int64_t)n * r->spec_cols + r->num_accepted_tokens[n] - 1]
+                    : r->state_indices[n];
     read_prior = load_slot > 0 && (r->has_initial_state ? r->has_initial_state[n] != 0 : 1);
   }
   const int64_t head_elems = (int64_t)dv * dk;

@@ -124,6 +124,18 @@ def test_shape_checks(lib, kw):
     assert mixed(lib, layer=big_layer(**kw)) == ERR["SHAPE"]
 
 
+def test_acceptance_aware_non_spec_rows(lib):
+    # a non-spec subset may carry the spec pair (the previous verify step's slots and acceptance)
+    aware = ns_rows(spec_state_indices=FAKE, num_accepted_tokens=FAKE, spec_cols=4)
+    assert mixed(lib, non_spec=aware, ws_bytes=16) == ERR["WORKSPACE"]
+    # ... still as a pair, with a valid column count that fits the rolled ring
+    assert mixed(lib, non_spec=ns_rows(spec_state_indices=FAKE, spec_cols=4)) == ERR["SPEC_PAIR"]
+    assert mixed(lib, non_spec=ns_rows(spec_state_indices=FAKE, num_accepted_tokens=FAKE, spec_cols=0)) == ERR["SHAPE"]
+    assert mixed(lib, non_spec=ns_rows(spec_state_indices=FAKE, num_accepted_tokens=FAKE, spec_cols=5)) == ERR["SHAPE"]
+    # the spec slot takes only spec rows, so aware rows there are refused
+    assert mixed(lib, spec=spec_rows(state_indices=FAKE, token_indx=FAKE)) == ERR["SPEC_PAIR"]
+
+
 def test_spec_cols_must_fit_the_conv_ring(lib):
     # state_len 6 with W = 4 holds at most 4 verify tokens per row in the rolled layout
     assert mixed(lib, spec=spec_rows(k=5, token_indx=FAKE)) == ERR["SHAPE"]
