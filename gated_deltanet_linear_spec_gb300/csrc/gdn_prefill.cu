@@ -46,13 +46,12 @@ constexpr uint32_t kKpLo = 49152;   //               bf16 lo image              
 constexpr uint32_t kQp = 65536;     // gamma q^ [t][dk] bf16 image                       16 KiB
 constexpr uint32_t kP = 81920;      // P    [t][s]   bf16 image                           8 KiB
 constexpr uint32_t kImgBytes = 90112;  // the images above: one bulk copy
-constexpr uint32_t kUt = 90112;     // U~   [t][dv]  fp32                                32 KiB
+constexpr uint32_t kUt = 90112;     // U~   [dv/32][t][32] fp32 (a quarter of dv each)  32 KiB
 constexpr uint32_t kMeta = 122880;  // gamma_c (fp32)
-constexpr uint32_t kScanCopy = kMeta + 16;  // what the scan kernel copies per chunk
-static_assert(kRecBytes >= kScanCopy && kUt == kImgBytes, "record layout");
+static_assert(kRecBytes >= kMeta + 16 && kUt == kImgBytes, "record layout");
 
-constexpr int kPrepSmem = 81920 + 1024;
-constexpr int kScanSmem = 98304 + (int)kScanCopy + 1024;
+constexpr int kAStride = 68;  // floats per row of A in shared memory (16-byte aligned rows)
+constexpr int kPrepSmem = 81920 + kCh * kAStride * 4 + 1024;
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -77,6 +76,26 @@ __device__ __forceinline__ void put4_pair(uint8_t* hi_img, uint8_t* lo_img, int 
   *reinterpret_cast<uint2*>(lo_img + off) = *reinterpret_cast<const uint2*>(l);
 }
 
+// Four consecutive activations (16-byte aligned fp32 or 8-byte aligned bf16) as fp32.
+__device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+  const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+// One fp32 value as a bf16 hi/lo pair at byte offset off of two images.
+__device__ __forceinline__ void put_pair(uint8_t* hi_img, uint8_t* lo_img, uint32_t off, float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+  *reinterpret_cast<__nv_bfloat16*>(hi_img + off) = hi;
+  *reinterpret_cast<__nv_bfloat16*>(lo_img + off) = lo;
+}
+
 __device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
   const float x = a + dt_bias;
   return -expf(A_log) * (x > 20.f ? x : log1pf(expf(x)));
@@ -90,15 +109,15 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
   uint8_t* sm = align1k(dyn_smem);
   uint8_t* qk_hi = sm;  // [q^; k^] [128][128] images (MMA 1)
   uint8_t* qk_lo = sm + 32768;
-  float* sA = reinterpret_cast<float*>(sm);           // A [64][65]      (after MMA 1)
-  float* sT = reinterpret_cast<float*>(sm + 16640);   // T [64][65]
-  uint8_t* kb_hi = sm;  // (beta gamma k^)^T [128][64]  (after T is imaged)
+  float* sA = reinterpret_cast<float*>(sm + 81920);  // A [64][kAStride]  (after MMA 1)
+  uint8_t* kb_hi = sm;  // (beta gamma k^)^T [128][64]  (after MMA 1)
   uint8_t* kb_lo = sm + 16384;
   uint8_t* vb_hi = sm + 32768;  // (beta v)^T [128][64]
   uint8_t* vb_lo = sm + 49152;
   uint8_t* t_hi = sm + 65536;  // T [64][64]
   uint8_t* t_lo = sm + 73728;
-  __shared__ float sG[kCh], sBeta[kCh], sRk[kCh];
+  __shared__ float sG[kCh], sBeta[kCh], sRk[kCh], sFk[kCh], sFp[kCh];
+  __shared__ float sMs[2][256];  // per-warp 16 x 16 scratch of the blocked solve
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tmem_base;
 
@@ -139,35 +158,37 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = tmem_base;
-  if (tid == 0) {
-    float acc = 0.f;
-    for (int t = 0; t < kCh; ++t) {
-      acc += sG[t];
-      sG[t] = acc;  // G_t, inclusive
+  if (warp == 0) {  // G_t = g_1 + .. + g_t (inclusive): lane l sums tokens 2l, 2l+1, then a warp scan
+    const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
+    float x = g0 + g1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
+    sG[2 * lane] = x - g1;
+    sG[2 * lane + 1] = x;
   }
   __syncthreads();
 
   // 2. q^ (scaled) and k^ rows of the [q^; k^] images, and the gamma q^ record rows; warp w
   //    takes tokens 16w .. 16w+15, four at a time so their loads are in flight together
-  for (int i0 = 0; i0 < 16; i0 += 4) {
-    float q[4][4], k[4][4];
+  for (int i0 = 0; i0 < 16; i0 += 8) {
+    float q[8][4], k[8][4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < 8; ++b) {
       const int t = warp * 16 + i0 + b;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) q[b][e] = k[b][e] = 0.f;
       if (t < nc) {
         const QT* row = qkv + (int64_t)(bos + t0 + t) * C;
+        load4(row + qoff + 4 * lane, q[b]);
+        load4(row + koff + 4 * lane, k[b]);
+      } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          q[b][e] = to_f32(row[qoff + 4 * lane + e]);
-          k[b][e] = to_f32(row[koff + 4 * lane + e]);
-        }
+        for (int e = 0; e < 4; ++e) q[b][e] = k[b][e] = 0.f;
       }
     }
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < 8; ++b) {
       const int t = warp * 16 + i0 + b;
       float sq = 0.f, sk = 0.f;
 #pragma unroll
@@ -211,6 +232,11 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
     }
     tc::commit(&bar);
   }
+  if (tid < kCh) {  // per-token factors of the k^T images: beta gamma / |k| and e^{G_c - G_s} / |k|
+    const float Gc = sG[kCh - 1];
+    sFk[tid] = sBeta[tid] * expf(sG[tid]) * sRk[tid];
+    sFp[tid] = tid < nc ? expf(Gc - sG[tid]) * sRk[tid] : 0.f;
+  }
   bool ok = __syncthreads_and(tc::mbar_wait(&bar, 0));
   if (ok) {
     tc::fence_after();
@@ -235,89 +261,167 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
     } else {
       const float bt = sBeta[t];
 #pragma unroll
-      for (int s = 0; s < kCh; ++s) {
-        const float kk = s < 32 ? v0[s & 31] : v1[s & 31];
-        sA[t * 65 + s] = s < t ? bt * expf(Gt - sG[s]) * kk : 0.f;
+      for (int s0 = 0; s0 < kCh; s0 += 4) {
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int s = s0 + e;
+          const float kk = s < 32 ? v0[s & 31] : v1[s & 31];
+          x[e] = s < t ? bt * expf(Gt - sG[s]) * kk : 0.f;
+        }
+        *reinterpret_cast<float4*>(sA + t * kAStride + s0) = make_float4(x[0], x[1], x[2], x[3]);
       }
     }
     __syncthreads();
 
-    // 5. T = (I + A)^-1, column s by thread s: T[t][s] = -sum_{s<=j<t} A[t][j] T[j][s]
-    if (tid < kCh) {
-      const int s = tid;
-      for (int t2 = 0; t2 < s; ++t2) sT[t2 * 65 + s] = 0.f;
-      sT[s * 65 + s] = 1.f;
-      for (int t2 = s + 1; t2 < kCh; ++t2) {
-        float acc0 = 0.f, acc1 = 0.f;
-        int j = s;
-        for (; j + 1 < t2; j += 2) {
-          acc0 = fmaf(sA[t2 * 65 + j], sT[j * 65 + s], acc0);
-          acc1 = fmaf(sA[t2 * 65 + j + 1], sT[(j + 1) * 65 + s], acc1);
+    if (warp < 2) {
+      // 5. T = (I + A)^-1 on warps 0-1 in 16 x 16 blocks: the diagonal blocks (I + A_bb)^-1 by
+      //    forward substitution, then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj in order of i - j.
+      //    T is kept transposed in the upper half of the A array: T[t][s] (t >= s) at sA[s][t]
+      //    (A is strictly lower, and A_ii is not read again once T_ii exists).
+      {
+        const int o = 16 * (2 * warp + (lane >> 4)), c = lane & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {  // entries at and above the diagonal of A are zero
+          float acc = r == c ? 1.f : 0.f;
+#pragma unroll
+          for (int m = 0; m < ((r + 3) & ~3); m += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(sA + (o + r) * kAStride + o + m);
+            acc = fmaf(-a.x, x[m], acc);
+            acc = fmaf(-a.y, x[m + 1], acc);
+            acc = fmaf(-a.z, x[m + 2], acc);
+            acc = fmaf(-a.w, x[m + 3], acc);
+          }
+          x[r] = acc;
         }
-        if (j < t2) acc0 = fmaf(sA[t2 * 65 + j], sT[j * 65 + s], acc0);
-        sT[t2 * 65 + s] = -(acc0 + acc1);
-      }
-    }
-    __syncthreads();
-    // 6a. T image (rows t, K = s): thread -> row tid/2, 32 columns
-    {
-      const int tt = tid >> 1, s0 = (tid & 1) * 32;
+        __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = sT[tt * 65 + s0 + 8 * j + e];
-        uint4 hi, lo;
-        tc::split8(x, hi, lo);
-        const uint32_t off = tc::img_off(tt, s0 + 8 * j, 1);
-        *reinterpret_cast<uint4*>(t_hi + off) = hi;
-        *reinterpret_cast<uint4*>(t_lo + off) = lo;
+        for (int r = 0; r < 16; ++r)
+          if (r >= c) sA[(o + c) * kAStride + o + r] = x[r];
       }
-    }
-    __syncthreads();  // T consumed; the region is reused below
-    // 6b. (beta gamma k^)^T and (beta v)^T images (shared memory) and the K'^T record images,
-    //     row d = tid; the column loads of 16 tokens are issued together
-    {
-      const int d = tid;
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      float* sM = sMs[warp];
+      const int c = lane & 15, r0 = (lane >> 4) * 8;
+#pragma unroll 1
+      for (int dist = 1; dist < 4; ++dist) {
+#pragma unroll 1
+        for (int i = dist + warp; i < 4; i += 2) {
+          const int j = i - dist;
+          float m8[8];
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) m8[rr] = 0.f;
+#pragma unroll 1
+          for (int k = j; k < i; ++k) {  // M = sum_k A_ik T_kj, rows r0.., column c
+#pragma unroll
+            for (int mm = 0; mm < 16; mm += 4) {
+              // T[16k+mm..][16j+c] sits transposed at row 16j+c; in the diagonal block only mm >= c
+              float4 tv = *reinterpret_cast<const float4*>(sA + (16 * j + c) * kAStride + 16 * k + mm);
+              if (k == j) {
+                tv.x = mm >= c ? tv.x : 0.f;
+                tv.y = mm + 1 >= c ? tv.y : 0.f;
+                tv.z = mm + 2 >= c ? tv.z : 0.f;
+                tv.w = mm + 3 >= c ? tv.w : 0.f;
+              }
+#pragma unroll
+              for (int rr = 0; rr < 8; ++rr) {
+                const float4 a = *reinterpret_cast<const float4*>(sA + (16 * i + r0 + rr) * kAStride + 16 * k + mm);
+                m8[rr] = fmaf(a.x, tv.x, m8[rr]);
+                m8[rr] = fmaf(a.y, tv.y, m8[rr]);
+                m8[rr] = fmaf(a.z, tv.z, m8[rr]);
+                m8[rr] = fmaf(a.w, tv.w, m8[rr]);
+              }
+            }
+          }
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) sM[(r0 + rr) * 16 + c] = m8[rr];
+          __syncwarp();
+          float acc[8];
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) acc[rr] = 0.f;
+#pragma unroll
+          for (int mm = 0; mm < 16; ++mm) {  // T_ij = -T_ii M;  T_ii[r][mm] (mm <= r) at row 16i+mm
+            const float4 t0 = *reinterpret_cast<const float4*>(sA + (16 * i + mm) * kAStride + 16 * i + r0);
+            const float4 t1 = *reinterpret_cast<const float4*>(sA + (16 * i + mm) * kAStride + 16 * i + r0 + 4);
+            const float tr[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+            const float mv = sM[mm * 16 + c];
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) acc[rr] = fmaf(mm <= r0 + rr ? tr[rr] : 0.f, mv, acc[rr]);
+          }
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) sA[(16 * j + c) * kAStride + 16 * i + r0 + rr] = -acc[rr];
+          __syncwarp();
+        }
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+      }
+      // 6a. T image (rows t, K = s): thread t of warps 0-1
+      {
+        const int t2 = tid;
+#pragma unroll
+        for (int g8 = 0; g8 < kCh; g8 += 8) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s2 = g8 + e;
+            x[e] = s2 <= t2 ? sA[s2 * kAStride + t2] : 0.f;
+          }
+          uint4 hi, lo;
+          tc::split8(x, hi, lo);
+          const uint32_t off = tc::img_off(t2, g8, 1);
+          *reinterpret_cast<uint4*>(t_hi + off) = hi;
+          *reinterpret_cast<uint4*>(t_lo + off) = lo;
+        }
+      }
+    } else {
+      // 6b. meanwhile: (beta gamma k^)^T and (beta v)^T images (shared memory) and the K'^T
+      //     record images, rows d and d + 64 of the thread; the loads of 16 tokens of both rows
+      //     are issued together
       const float Gc = sG[kCh - 1];
+      const int d = tid - 64;
 #pragma unroll 1
       for (int s0 = 0; s0 < kCh; s0 += 16) {
-        float kr[16], vr[16];
+        float kr[2][16], vr[2][16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int s = s0 + e;
-          kr[e] = vr[e] = 0.f;
-          if (s < nc) {
-            const QT* row = qkv + (int64_t)(bos + t0 + s) * C;
-            kr[e] = to_f32(row[koff + d]);
-            vr[e] = to_f32(row[voff + d]);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            kr[r][e] = vr[r][e] = 0.f;
+            if (s < nc) {
+              const QT* row = qkv + (int64_t)(bos + t0 + s) * C;
+              kr[r][e] = to_f32(row[koff + d + 64 * r]);
+              vr[r][e] = to_f32(row[voff + d + 64 * r]);
+            }
           }
         }
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float xk[8], xv[8], xp[8];
+        for (int r = 0; r < 2; ++r)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = s0 + 8 * half + e;
-            const float kn = kr[8 * half + e] * sRk[s], bs = sBeta[s];
-            xk[e] = bs * expf(sG[s]) * kn;
-            xv[e] = bs * vr[8 * half + e];
-            xp[e] = s < nc ? expf(Gc - sG[s]) * kn : 0.f;
+          for (int half = 0; half < 2; ++half) {
+            float xk[8], xv[8], xp[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int s = s0 + 8 * half + e;
+              xk[e] = sFk[s] * kr[r][8 * half + e];
+              xv[e] = sBeta[s] * vr[r][8 * half + e];
+              xp[e] = sFp[s] * kr[r][8 * half + e];
+            }
+            uint4 hi, lo;
+            const uint32_t off = tc::img_off(d + 64 * r, s0 + 8 * half, 1);
+            tc::split8(xk, hi, lo);
+            *reinterpret_cast<uint4*>(kb_hi + off) = hi;
+            *reinterpret_cast<uint4*>(kb_lo + off) = lo;
+            tc::split8(xv, hi, lo);
+            *reinterpret_cast<uint4*>(vb_hi + off) = hi;
+            *reinterpret_cast<uint4*>(vb_lo + off) = lo;
+            tc::split8(xp, hi, lo);
+            *reinterpret_cast<uint4*>(rec + kKpHi + off) = hi;
+            *reinterpret_cast<uint4*>(rec + kKpLo + off) = lo;
           }
-          uint4 hi, lo;
-          const uint32_t off = tc::img_off(d, s0 + 8 * half, 1);
-          tc::split8(xk, hi, lo);
-          *reinterpret_cast<uint4*>(kb_hi + off) = hi;
-          *reinterpret_cast<uint4*>(kb_lo + off) = lo;
-          tc::split8(xv, hi, lo);
-          *reinterpret_cast<uint4*>(vb_hi + off) = hi;
-          *reinterpret_cast<uint4*>(vb_lo + off) = lo;
-          tc::split8(xp, hi, lo);
-          *reinterpret_cast<uint4*>(rec + kKpHi + off) = hi;
-          *reinterpret_cast<uint4*>(rec + kKpLo + off) = lo;
-        }
       }
-      if (tid == 0) *reinterpret_cast<float*>(rec + kMeta) = expf(Gc);
+      if (tid == 64) *reinterpret_cast<float*>(rec + kMeta) = expf(Gc);
     }
     tc::fence_async_smem();
     tc::fence_before();
@@ -359,7 +463,7 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
         }
         tc::tmem_ld32(tc::tmem_lane_col(tmem, warp, 128 + 32 * half), w);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ut[(32 * half + i) * kD + d] = w[i];
+        for (int i = 0; i < 32; ++i) ut[((d >> 5) * kCh + 32 * half + i) * 32 + (d & 31)] = w[i];
       }
       __syncthreads();
       const uint4* src = reinterpret_cast<const uint4*>(sm);
@@ -379,22 +483,41 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
 }
 
 // ------------------------------------------------------------------------------------------
-// Scan: one CTA per (row, v-head); 128 threads, thread d owns row d of the state.
+// Scan: one CTA per (row, v-head, quarter of dv); 128 threads.  The state rows are independent
+// given the chunk inputs (U, O and the new state of dv row j read only row j of S_0), so each
+// CTA carries 32 rows of S.  It keeps S^T (lane = dk, column = its 32 dv) in TMEM so the state
+// update is an M = 128 MMA:  S_c^T = gamma_c S_0^T + K'^T U.  U and O are M = 64 accumulators
+// (row t of a 64-row accumulator sits in TMEM lane t % 16 + 32 (t / 16)).
+//   U   = U~ - W S_0^T          A = -W [t][dk],     B = S_0 [dv][dk]      (three passes)
+//   O   = (gamma q^) S_0^T      A = gamma q^ [t][dk], B = S_0 [dv][dk]    (one pass)
+//   S^T += K'^T U               A = K'^T [dk][s],    B = U^T [dv][s]      (three passes)
+//   O  += P U                   A = P [t][s],        B = U^T [dv][s]      (one pass)
+// Chunk records arrive by bulk copy into two buffers, two chunks ahead.
+constexpr int kQuarters = kD / 32;
+constexpr uint32_t kBufUt = kImgBytes;          // this CTA's quarter of U~, [t][32] fp32
+constexpr uint32_t kBufMeta = kImgBytes + 8192;  // gamma_c
+constexpr uint32_t kBufBytes = kBufMeta + 1024;  // 1 KiB-aligned buffers
+constexpr uint32_t kBufCopy = kImgBytes + 8192 + 16;
+constexpr uint32_t kSImg = 2 * kBufBytes;        // S_0 [32][128] hi, lo: 8 KiB each
+constexpr uint32_t kUImg = kSImg + 16384;        // U^T [32][64] hi, lo: 4 KiB each
+constexpr int kScanSmemNew = (int)kUImg + 8192 + 1024;
+static_assert(kScanSmemNew <= 232448, "scan shared memory");
+
 __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch p) {
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* sm = align1k(dyn_smem);
-  uint8_t* s_hi = sm;  // S [dv][dk] images (A operand), 32 KiB each
-  uint8_t* s_lo = sm + 32768;
-  uint8_t* u_hi = sm + 65536;  // U^T [dv][s] images, 16 KiB each; then the output staging
-  uint8_t* u_lo = sm + 81920;
-  uint8_t* ops = sm + 98304;  // the chunk record: images, U~, gamma_c (kScanCopy bytes)
-  __nv_bfloat16* o_stage = reinterpret_cast<__nv_bfloat16*>(u_hi);  // [t][dv]
-  __shared__ __align__(8) uint64_t bar_mma, bar_tma;
+  uint8_t* s_hi = sm + kSImg;
+  uint8_t* s_lo = s_hi + 8192;
+  uint8_t* u_hi = sm + kUImg;
+  uint8_t* u_lo = u_hi + 4096;
+  // one barrier per commit point, each committed and waited once per chunk (so a wait is never
+  // more than one phase behind): U ready; state update (and the first O half) done; O done
+  __shared__ __align__(8) uint64_t bar_mma[3], bar_tma[2];
   __shared__ uint32_t tmem_base;
   __shared__ int sGt[kCh];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x;
+  const int h = blockIdx.x / kQuarters, q = blockIdx.x % kQuarters;
   const int n = p.first_row + blockIdx.y;
   const int base_unit = units_before(p.rows, p.first_row, n, kCh);
   const int bos = __ldg(p.rows.qsl + n), eos = __ldg(p.rows.qsl + n + 1);
@@ -404,203 +527,195 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   int slot = __ldg(p.rows.state_idx + n);
   const int load_slot = non_spec_load_slot(p.rows, n);
   if (load_slot < 0) {  // acceptance-aware row with num_accepted out of range
-    if (tid == 0 && h == 0) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
+    if (tid == 0 && blockIdx.x == 0) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
     return;
   }
   bool read_prior = load_slot > 0 && (p.rows.has_init == nullptr || __ldg(p.rows.has_init + n) != 0);
   if (slot >= p.num_slots || load_slot >= p.num_slots) {
-    if (tid == 0 && h == 0) set_status(p.status, GDN_STATUS_SLOT_RANGE);
+    if (tid == 0 && blockIdx.x == 0) set_status(p.status, GDN_STATUS_SLOT_RANGE);
     if (slot >= p.num_slots) slot = 0;
     read_prior = false;
   }
-  const int d = 32 * warp + lane;
-  float* gS = p.ssm_pool + ((int64_t)slot * p.Hv + h) * kD * kD + (int64_t)d * kD;
-  const float* gS0 = p.ssm_pool + ((int64_t)(read_prior ? load_slot : 0) * p.Hv + h) * kD * kD + (int64_t)d * kD;
+  const int dk = 32 * warp + lane;  // this thread's TMEM lane of S^T
+  const int dv0 = 32 * q;
+  // element (dv0 + j, dk) of the state is at base + j * kD
+  float* gS = p.ssm_pool + ((int64_t)slot * p.Hv + h) * kD * kD + (int64_t)dv0 * kD + dk;
+  const float* gS0 = p.ssm_pool + ((int64_t)(read_prior ? load_slot : 0) * p.Hv + h) * kD * kD + (int64_t)dv0 * kD + dk;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 
-  if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
+  if (warp == 0) tc::tmem_alloc(&tmem_base, 128);
   if (tid == 32) {
-    tc::mbar_init(&bar_mma, 1);
-    tc::mbar_init(&bar_tma, 1);
+    for (int i = 0; i < 3; ++i) tc::mbar_init(&bar_mma[i], 1);
+    tc::mbar_init(&bar_tma[0], 1);
+    tc::mbar_init(&bar_tma[1], 1);
     tc::mbar_init_fence();
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tS = tmem_base, tU = tmem_base + 128, tO = tmem_base + 192;
-  auto record = [&](int c) { return p.ws + ((size_t)(base_unit + c) * p.Hv + h) * kRecBytes; };
-
-  // initial state: fp32 master in TMEM (lane d) and its hi/lo images (row d)
-  for (int c0 = 0; c0 < kD; c0 += 32) {
-    float v[32];
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      float4 f = read_prior ? *reinterpret_cast<const float4*>(gS0 + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-      v[j] = f.x; v[j + 1] = f.y; v[j + 2] = f.z; v[j + 3] = f.w;
-    }
-    tc::tmem_st32(tc::tmem_lane_col(tS, warp, c0), v);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 hi, lo;
-      tc::split8(v + 8 * j, hi, lo);
-      const uint32_t off = tc::img_off(d, c0 + 8 * j, 2);
-      *reinterpret_cast<uint4*>(s_hi + off) = hi;
-      *reinterpret_cast<uint4*>(s_lo + off) = lo;
-    }
-  }
-  tc::tmem_st_wait();
-  tc::fence_async_smem();
+  const uint32_t tS = tmem_base, tU = tmem_base + 32, tO = tmem_base + 64;
+  auto issue = [&](int c) {  // chunk c's record -> buffer c & 1
+    const uint8_t* rec = p.ws + ((size_t)(base_unit + c) * p.Hv + h) * kRecBytes;
+    uint8_t* buf = sm + (c & 1) * kBufBytes;
+    uint64_t* bar = &bar_tma[c & 1];
+    tc::expect_tx(bar, kBufCopy);
+    tc::bulk_g2s(buf, rec, kImgBytes, bar);
+    tc::bulk_g2s(buf + kBufUt, rec + kUt + q * 8192, 8192, bar);
+    tc::bulk_g2s(buf + kBufMeta, rec + kMeta, 16, bar);
+  };
   if (tid == 0) {
-    tc::expect_tx(&bar_tma, kScanCopy);
-    tc::bulk_g2s(ops, record(0), kScanCopy, &bar_tma);
+    issue(0);
+    if (nch > 1) issue(1);
   }
+  int tma_issued[2] = {1, nch > 1 ? 1 : 0}, tma_done[2] = {0, 0};
+  int mma_commits[3] = {0, 0, 0}, mma_done[3] = {0, 0, 0};
 
-  bool ok = true;
-  uint32_t tma_phase = 0, mma_phase = 0;
+  // initial state: images of S_0 (unscaled) and gamma_0 S_0^T in TMEM
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = read_prior ? gS0[(int64_t)j * kD] : 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) put_pair(s_hi, s_lo, tc::img_off(j, dk, 2), v[j]);
+  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma[0], 0));
+  tma_done[0] = 1;
+  if (ok) {
+    const float g0 = *reinterpret_cast<const float*>(sm + kBufMeta);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= g0;
+    tc::tmem_st32(tc::tmem_lane_col(tS, warp, 0), v);
+    tc::tmem_st_wait();
+  }
+  tc::fence_async_smem();
+  tc::fence_before();
+  __syncthreads();
+
   for (int c = 0; c < nch && ok; ++c) {
+    const int b = c & 1;
+    uint8_t* buf = sm + b * kBufBytes;
     if (tid < kCh) {
       const int t = c * kCh + tid;
       sGt[tid] = t < L ? global_token(p.rows, bos + t, p.num_global, p.status) : -1;
     }
-    ok = __syncthreads_and(tc::mbar_wait(&bar_tma, tma_phase));
-    tma_phase ^= 1;
+    // U = -W S_0^T (three passes) -> commit;  O = (gamma q^) S_0^T
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t id = tc::idesc_bf16(64, 32);
+      const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi), sl = tc::smem_addr(s_lo);
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
+        tc::mma3(tU, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc(sh + off, 2048),
+                 tc::sdesc(sl + off, 2048), id, s == 0);
+      }
+      tc::commit(&bar_mma[0]);
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
+        tc::mma(tO, tc::sdesc(bb + kQp + off, 2048), tc::sdesc(sh + off, 2048), id, s > 0 ? 1u : 0u);
+      }
+    }
+    ++mma_commits[0];
+    ok = __syncthreads_and(tc::mbar_wait(&bar_mma[0], mma_done[0] & 1));
+    ++mma_done[0];
     if (!ok) break;
-    // U accumulator <- U~^T (row d), and S <- gamma_c S (this chunk's MMAs read the old S images)
+    tc::fence_after();
+    // U += U~; U^T images (row = dv, column = t)
     {
-      const float gamma_c = *reinterpret_cast<const float*>(ops + kMeta);
-      const float* ut = reinterpret_cast<const float*>(ops + kUt);
-      for (int half = 0; half < 2; ++half) {
-        float v[32];
+      float u[32];
+      tc::tmem_ld32(tc::tmem_lane_col(tU, warp, 0), u);
+      if (lane < 16) {
+        const int t = 16 * warp + lane;
+        const float4* ut = reinterpret_cast<const float4*>(buf + kBufUt) + t * 8;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = ut[(32 * half + i) * kD + d];
-        tc::tmem_st32(tc::tmem_lane_col(tU, warp, 32 * half), v);
-      }
-      for (int c0 = 0; c0 < kD; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(tc::tmem_lane_col(tS, warp, c0), v);
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 f = ut[j4];
+          u[4 * j4] += f.x; u[4 * j4 + 1] += f.y; u[4 * j4 + 2] += f.z; u[4 * j4 + 3] += f.w;
+        }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= gamma_c;
-        tc::tmem_st32(tc::tmem_lane_col(tS, warp, c0), v);
-      }
-      tc::tmem_st_wait();
-    }
-    tc::fence_before();
-    __syncthreads();
-    // U^T += S (-W)^T (three passes) -> commit;  O^T = S q'^T
-    if (tid == 0) {
-      tc::fence_after();
-      const uint32_t id64 = tc::idesc_bf16(128, 64);
-      const uint32_t sh = tc::smem_addr(s_hi), sl = tc::smem_addr(s_lo), ob = tc::smem_addr(ops);
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
-        tc::mma3(tU, tc::sdesc(sh + off, 2048), tc::sdesc(sl + off, 2048), tc::sdesc(ob + kWnHi + off, 2048),
-                 tc::sdesc(ob + kWnLo + off, 2048), id64, false);
-      }
-      tc::commit(&bar_mma);
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
-        tc::mma(tO, tc::sdesc(sh + off, 2048), tc::sdesc(ob + kQp + off, 2048), id64, s > 0 ? 1u : 0u);
-      }
-    }
-    ok = __syncthreads_and(tc::mbar_wait(&bar_mma, mma_phase));
-    mma_phase ^= 1;
-    if (!ok) break;
-    tc::fence_after();
-    // U^T images (row d)
-    for (int half = 0; half < 2; ++half) {
-      float v[32];
-      tc::tmem_ld32(tc::tmem_lane_col(tU, warp, 32 * half), v);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 hi, lo;
-        tc::split8(v + 8 * j, hi, lo);
-        const uint32_t off = tc::img_off(d, 32 * half + 8 * j, 1);
-        *reinterpret_cast<uint4*>(u_hi + off) = hi;
-        *reinterpret_cast<uint4*>(u_lo + off) = lo;
+        for (int j = 0; j < 32; ++j) put_pair(u_hi, u_lo, tc::img_off(j, t, 1), u[j]);
       }
     }
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // S += U^T K' (three passes, N = 128) -> commit;  O^T += U^T P^T -> commit
+    // S^T += K'^T U (three passes) -> commit;  O += P U -> commit
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t id64 = tc::idesc_bf16(128, 64), id128 = tc::idesc_bf16(128, 128);
-      const uint32_t uh = tc::smem_addr(u_hi), ul = tc::smem_addr(u_lo), ob = tc::smem_addr(ops);
+      const uint32_t id64 = tc::idesc_bf16(64, 32), id128 = tc::idesc_bf16(128, 32);
+      const uint32_t bb = tc::smem_addr(buf), uh = tc::smem_addr(u_hi), ul = tc::smem_addr(u_lo);
       for (int s = 0; s < 4; ++s) {
         const uint32_t off = s * 32;
-        tc::mma3(tS, tc::sdesc(uh + off, 1024), tc::sdesc(ul + off, 1024), tc::sdesc(ob + kKpHi + off, 1024),
-                 tc::sdesc(ob + kKpLo + off, 1024), id128, false);
+        tc::mma3(tS, tc::sdesc(bb + kKpHi + off, 1024), tc::sdesc(bb + kKpLo + off, 1024), tc::sdesc(uh + off, 1024),
+                 tc::sdesc(ul + off, 1024), id128, false);
       }
-      tc::commit(&bar_mma);
+      tc::commit(&bar_mma[1]);
       for (int s = 0; s < 4; ++s) {
         const uint32_t off = s * 32;
-        tc::mma(tO, tc::sdesc(uh + off, 1024), tc::sdesc(ob + kP + off, 1024), id64, 1u);
+        tc::mma(tO, tc::sdesc(bb + kP + off, 1024), tc::sdesc(uh + off, 1024), id64, 1u);
       }
-      tc::commit(&bar_mma);
+      tc::commit(&bar_mma[2]);
     }
-    ok = __syncthreads_and(tc::mbar_wait(&bar_mma, mma_phase));
-    mma_phase ^= 1;
+    ++mma_commits[1];
+    ++mma_commits[2];
+    ok = __syncthreads_and(tc::mbar_wait(&bar_mma[1], mma_done[1] & 1));
+    ++mma_done[1];
     if (!ok) break;
     tc::fence_after();
-    // images of the new state for the next chunk (every MMA that read the old ones is done)
-    for (int c0 = 0; c0 < kD; c0 += 32) {
-      float v[32];
-      tc::tmem_ld32(tc::tmem_lane_col(tS, warp, c0), v);
+    // the new state: images for the next chunk, then gamma_{c+1} S^T back into TMEM
+    tc::tmem_ld32(tc::tmem_lane_col(tS, warp, 0), v);
+    bool tma_ok = true;
+    if (c + 1 < nch) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 hi, lo;
-        tc::split8(v + 8 * j, hi, lo);
-        const uint32_t off = tc::img_off(d, c0 + 8 * j, 2);
-        *reinterpret_cast<uint4*>(s_hi + off) = hi;
-        *reinterpret_cast<uint4*>(s_lo + off) = lo;
-      }
+      for (int j = 0; j < 32; ++j) put_pair(s_hi, s_lo, tc::img_off(j, dk, 2), v[j]);
+      const int nb = (c + 1) & 1;
+      tma_ok = tc::mbar_wait(&bar_tma[nb], tma_done[nb] & 1);
+      ++tma_done[nb];
+      const float gn = *reinterpret_cast<const float*>(sm + nb * kBufBytes + kBufMeta);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= gn;
+      tc::tmem_st32(tc::tmem_lane_col(tS, warp, 0), v);
+    } else if (slot > 0) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) gS[(int64_t)j * kD] = v[j];
     }
-    ok = __syncthreads_and(tc::mbar_wait(&bar_mma, mma_phase));
-    mma_phase ^= 1;
+    const bool mma_ok = tc::mbar_wait(&bar_mma[2], mma_done[2] & 1);
+    ok = __syncthreads_and(tma_ok && mma_ok);
+    ++mma_done[2];
     if (!ok) break;
     tc::fence_after();
-    if (tid == 0 && c + 1 < nch) {  // the record is consumed: prefetch the next chunk's
-      tc::expect_tx(&bar_tma, kScanCopy);
-      tc::bulk_g2s(ops, record(c + 1), kScanCopy, &bar_tma);
+    if (tid == 0 && c + 2 < nch) {  // this buffer is consumed: fetch chunk c + 2 into it
+      issue(c + 2);
     }
-    // outputs: O^T row d, column t -> staged [t][d] -> 16-byte stores to out[token][h][:]
-    for (int half = 0; half < 2; ++half) {
-      float v[32];
-      tc::tmem_ld32(tc::tmem_lane_col(tO, warp, 32 * half), v);
+    if (c + 2 < nch) ++tma_issued[b];
+    // outputs: row t of O -> 32 bf16 of out[token][h][dv0 ..]
+    {
+      float o[32];
+      tc::tmem_ld32(tc::tmem_lane_col(tO, warp, 0), o);
+      if (lane < 16) {
+        const int gt = sGt[16 * warp + lane];
+        if (gt >= 0) {
+          uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)gt * p.Hv + h) * kD + dv0);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o_stage[(32 * half + i) * kD + d] = __float2bfloat16_rn(v[i]);
+          for (int i = 0; i < 4; ++i) dst[i] = tc::pack8(o + 8 * i);
+        }
+      }
     }
+    tc::tmem_st_wait();
     tc::fence_async_smem();
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int idx = tid + 128 * k;  // 64 tokens x 16 words
-      const int t = idx >> 4, w = idx & 15;
-      const int gt = sGt[t];
-      if (gt >= 0)
-        *reinterpret_cast<uint4*>(out + ((int64_t)gt * p.Hv + h) * kD + 8 * w) =
-            *reinterpret_cast<const uint4*>(o_stage + t * kD + 8 * w);
-    }
+    tc::fence_before();
     __syncthreads();
   }
 
   if (!ok) {
     if (tid == 0) set_status(p.status, GDN_STATUS_WAIT_TIMEOUT);
-    tc::mbar_wait(&bar_mma, mma_phase);  // bounded drains of anything still in flight
-    tc::mbar_wait(&bar_tma, tma_phase);
-  } else if (slot > 0) {
-    for (int c0 = 0; c0 < kD; c0 += 32) {
-      float v[32];
-      tc::tmem_ld32(tc::tmem_lane_col(tS, warp, c0), v);
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(gS + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-    }
+    // bounded drains of anything still in flight (the wait that failed included) before TMEM
+    // and shared memory are released
+    for (int i = 0; i < 3; ++i)
+      for (int k = mma_done[i] > 0 ? mma_done[i] - 1 : 0; k < mma_commits[i]; ++k) tc::mbar_wait(&bar_mma[i], k & 1);
+    for (int bb = 0; bb < 2; ++bb)
+      for (int k = tma_done[bb] > 0 ? tma_done[bb] - 1 : 0; k < tma_issued[bb]; ++k) tc::mbar_wait(&bar_tma[bb], k & 1);
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem_base, 128);
 }
 
 template <typename QT>
@@ -627,11 +742,11 @@ cudaError_t launch_prefill(const PrefillLaunch& p, gdn_dtype qkv_dtype, int unit
   if (e != cudaSuccess) return e;
   static bool configured = false;
   if (!configured) {
-    e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+    e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmemNew);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  chunk_scan_kernel<<<dim3(p.Hv, p.num_rows), 128, kScanSmem, s>>>(p);
+  chunk_scan_kernel<<<dim3(p.Hv * kQuarters, p.num_rows), 128, kScanSmemNew, s>>>(p);
   return cudaGetLastError();
 }
 

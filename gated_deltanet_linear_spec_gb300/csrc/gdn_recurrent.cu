@@ -103,15 +103,19 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   // Reading a valid slot is harmless even when the row turns out to be skipped.
   const int32_t bos = __ldg(R.qsl + n), eos = __ldg(R.qsl + n + 1);
   int load_slot = 0, na = 1;
-  bool read_prior;
+  bool read_prior, bad_accept = false;
   if (R.is_spec) {
     na = __ldg(R.num_acc + n);
     const bool na_ok = na >= 1 && na <= R.spec_cols;
     load_slot = na_ok ? __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1) : 0;
     read_prior = load_slot > 0;
   } else {
-    load_slot = non_spec_load_slot(R, n);
-    if (load_slot < 0) na = 0;  // acceptance out of range: flagged below
+    load_slot = __ldg(R.state_idx + n);
+    if (R.num_acc) {  // acceptance-aware row: the slot of its last accepted token
+      const int a = __ldg(R.num_acc + n);
+      bad_accept = a < 1 || a > R.spec_cols;
+      load_slot = bad_accept ? 0 : __ldg(R.spec_idx + (int64_t)n * R.spec_cols + a - 1);
+    }
     read_prior = load_slot > 0 && (R.has_init == nullptr || __ldg(R.has_init + n) != 0);
   }
   const bool slot_ok = load_slot < p.num_slots;
@@ -138,7 +142,8 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   if (bos < 0 || eos < bos || eos > R.num_tokens) skip = GDN_STATUS_ROW_RANGE;
   else if (L == 0) skip = 0x80000000u;
   else if (R.is_spec && L > R.spec_cols) skip = GDN_STATUS_ROW_RANGE;
-  else if ((R.is_spec || R.num_acc) && (na < 1 || na > R.spec_cols)) skip = GDN_STATUS_NUM_ACCEPTED;
+  else if (R.is_spec && (na < 1 || na > R.spec_cols)) skip = GDN_STATUS_NUM_ACCEPTED;
+  else if (bad_accept) skip = GDN_STATUS_NUM_ACCEPTED;
   if (skip) {
     if (reporter && skip != 0x80000000u) set_status(p.status, skip);
     return;
