@@ -487,7 +487,8 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
 // given the chunk inputs (U, O and the new state of dv row j read only row j of S_0), so each
 // CTA carries 32 rows of S.  It keeps S^T (lane = dk, column = its 32 dv) in TMEM so the state
 // update is an M = 128 MMA:  S_c^T = gamma_c S_0^T + K'^T U.  U and O are M = 64 accumulators
-// (row t of a 64-row accumulator sits in TMEM lane t % 16 + 32 (t / 16)).
+// (row t of a 64-row accumulator sits in TMEM lane t % 16 + 32 (t / 16)); TMEM columns: S^T
+// [0, 32), U [32, 64), O of even / odd chunks [64, 96) / [96, 128).
 //   U   = U~ - W S_0^T          A = -W [t][dk],     B = S_0 [dv][dk]      (three passes)
 //   O   = (gamma q^) S_0^T      A = gamma q^ [t][dk], B = S_0 [dv][dk]    (one pass)
 //   S^T += K'^T U               A = K'^T [dk][s],    B = U^T [dv][s]      (three passes)
@@ -514,7 +515,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   // more than one phase behind): U ready; state update (and the first O half) done; O done
   __shared__ __align__(8) uint64_t bar_mma[3], bar_tma[2];
   __shared__ uint32_t tmem_base;
-  __shared__ int sGt[kCh];
+  __shared__ int sGt[2][kCh];  // global tokens of the chunk whose outputs are pending
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x / kQuarters, q = blockIdx.x % kQuarters;
@@ -553,7 +554,20 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tS = tmem_base, tU = tmem_base + 32, tO = tmem_base + 64;
+  // O alternates between two accumulators: chunk c's outputs are drained while chunk c + 1 runs
+  const uint32_t tS = tmem_base, tU = tmem_base + 32, tO0 = tmem_base + 64;
+  auto store_outputs = [&](int c) {  // row t of O -> 32 bf16 of out[token][h][dv0 ..]
+    float o[32];
+    tc::tmem_ld32(tc::tmem_lane_col(tO0 + 32 * (c & 1), warp, 0), o);
+    if (lane < 16) {
+      const int gt = sGt[c & 1][16 * warp + lane];
+      if (gt >= 0) {
+        uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)gt * p.Hv + h) * kD + dv0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = tc::pack8(o + 8 * i);
+      }
+    }
+  };
   auto issue = [&](int c) {  // chunk c's record -> buffer c & 1
     const uint8_t* rec = p.ws + ((size_t)(base_unit + c) * p.Hv + h) * kRecBytes;
     uint8_t* buf = sm + (c & 1) * kBufBytes;
@@ -594,8 +608,9 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     uint8_t* buf = sm + b * kBufBytes;
     if (tid < kCh) {
       const int t = c * kCh + tid;
-      sGt[tid] = t < L ? global_token(p.rows, bos + t, p.num_global, p.status) : -1;
+      sGt[b][tid] = t < L ? global_token(p.rows, bos + t, p.num_global, p.status) : -1;
     }
+    const uint32_t tO = tO0 + 32 * b;
     // U = -W S_0^T (three passes) -> commit;  O = (gamma q^) S_0^T
     if (tid == 0) {
       tc::fence_after();
@@ -613,6 +628,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
       }
     }
     ++mma_commits[0];
+    if (c > 0) store_outputs(c - 1);  // while the U products run
     ok = __syncthreads_and(tc::mbar_wait(&bar_mma[0], mma_done[0] & 1));
     ++mma_done[0];
     if (!ok) break;
@@ -685,19 +701,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
       issue(c + 2);
     }
     if (c + 2 < nch) ++tma_issued[b];
-    // outputs: row t of O -> 32 bf16 of out[token][h][dv0 ..]
-    {
-      float o[32];
-      tc::tmem_ld32(tc::tmem_lane_col(tO, warp, 0), o);
-      if (lane < 16) {
-        const int gt = sGt[16 * warp + lane];
-        if (gt >= 0) {
-          uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)gt * p.Hv + h) * kD + dv0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = tc::pack8(o + 8 * i);
-        }
-      }
-    }
+    if (c + 1 == nch) store_outputs(c);
     tc::tmem_st_wait();
     tc::fence_async_smem();
     tc::fence_before();
