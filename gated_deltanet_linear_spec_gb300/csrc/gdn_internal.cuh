@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "gdn.h"
 
 namespace gdn {
@@ -174,6 +176,21 @@ __device__ __forceinline__ int units_before(const RowsDev& r, int first, int n, 
 }
 
 // ---- launch plumbing (host) ----------------------------------------------------------------
+
+// Runs `set` (a kernel attribute call, which applies to the current device's context) once per
+// device; safe to call from several host threads (a racing first call just repeats `set`).
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<uint64_t>& done, F set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return set();
+  const uint64_t bit = uint64_t(1) << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 inline RowsDev rows_dev(const gdn_rows* r) {
   RowsDev d{};

@@ -724,12 +724,11 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
 
 template <typename QT>
 cudaError_t launch_prep(const PrefillLaunch& p, int units, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = once_per_device(configured, [] {
+    return cudaFuncSetAttribute(chunk_prep_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  });
+  if (e != cudaSuccess) return e;
   chunk_prep_kernel<QT><<<dim3(units, p.Hv), 128, kPrepSmem, s>>>(p);
   return cudaGetLastError();
 }
@@ -744,12 +743,11 @@ cudaError_t launch_prefill(const PrefillLaunch& p, gdn_dtype qkv_dtype, int unit
   if (p.num_rows <= 0 || units_upper <= 0) return cudaSuccess;
   cudaError_t e = qkv_dtype == GDN_F32 ? launch_prep<float>(p, units_upper, s) : launch_prep<__nv_bfloat16>(p, units_upper, s);
   if (e != cudaSuccess) return e;
-  static bool configured = false;
-  if (!configured) {
-    e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmemNew);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  e = once_per_device(configured, [] {
+    return cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmemNew);
+  });
+  if (e != cudaSuccess) return e;
   chunk_scan_kernel<<<dim3(p.Hv * kQuarters, p.num_rows), 128, kScanSmemNew, s>>>(p);
   return cudaGetLastError();
 }
