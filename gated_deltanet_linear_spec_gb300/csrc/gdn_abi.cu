@@ -6,6 +6,7 @@
 // kernel", Changes, gdn_attn_interface.cpp bullet), and a mixed batch only has to conserve
 // tokens, not be rectangular ("[XE2] Support MTP of QWEN model", commit message).  Nothing here
 // reads device memory, so every call is stream-ordered and can be captured in a CUDA graph.
+#include <nvtx3/nvToolsExt.h>
 #include <limits.h>
 #include <math.h>
 #include <stdint.h>
@@ -165,6 +166,13 @@ RecLaunch rec_args(const gdn_layer_desc* d, const gdn_layer_params* prm, const g
 
 }  // namespace
 
+// A named NVTX range around each compute entry point (shows in Nsight timelines; without a tool
+// attached the push and pop are no-ops).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 extern "C" {
 
 const char* gdn_status_string(int code) {
@@ -198,6 +206,7 @@ size_t gdn_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* non_spec
 int gdn_conv_update(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
                     const void* x, int32_t num_global_tokens, const gdn_rows* rows, void* y, gdn_dtype y_dtype,
                     uint32_t* d_status, void* stream) {
+  NvtxRange nvtx_range("gdn_conv_update");
   int rc;
   if ((rc = check_layer(layer)) || (rc = check_params(params, true)) || (rc = check_pools(pools, true)) ||
       (rc = check_rows(layer, rows)))
@@ -220,6 +229,7 @@ int gdn_conv_update(const gdn_layer_desc* layer, const gdn_layer_params* params,
 int gdn_recurrent_step(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
                        const void* qkv, gdn_dtype qkv_dtype, const void* a, const void* b, int32_t num_global_tokens,
                        const gdn_rows* rows, void* out, uint32_t* d_status, void* stream) {
+  NvtxRange nvtx_range("gdn_recurrent_step");
   int rc;
   if ((rc = check_layer(layer)) || (rc = check_params(params, false)) || (rc = check_pools(pools, false)) ||
       (rc = check_rows(layer, rows)))
@@ -242,6 +252,7 @@ int gdn_chunk_prefill(const gdn_layer_desc* layer, const gdn_layer_params* param
                       const void* qkv, gdn_dtype qkv_dtype, const void* a, const void* b, int32_t num_global_tokens,
                       const gdn_rows* rows, int32_t chunk_size, void* out, void* workspace, size_t workspace_bytes,
                       uint32_t* d_status, void* stream) {
+  NvtxRange nvtx_range("gdn_chunk_prefill");
   int rc;
   if ((rc = check_layer(layer)) || (rc = check_params(params, false)) || (rc = check_pools(pools, false)) ||
       (rc = check_rows(layer, rows)))
@@ -272,6 +283,7 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
                     const void* x, const void* a, const void* b, int32_t num_actual_tokens, const gdn_rows* non_spec,
                     int32_t num_decodes, int32_t num_prefills, const gdn_rows* spec, void* out, void* workspace,
                     size_t workspace_bytes, uint32_t* d_status, void* stream) {
+  NvtxRange nvtx_range("gdn_mixed_batch");
   int rc;
   if ((rc = check_layer(layer)) || (rc = check_params(params, true)) || (rc = check_pools(pools, true)) ||
       (rc = check_rows(layer, non_spec)) || (rc = check_rows(layer, spec)))
