@@ -246,6 +246,67 @@ def timed(fn, steps, flush, stream):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def run_sweep(args) -> int:
+    """The throughput sweep on one GPU: spec verify at drafts in {1, 2, 4} x batch in {1, 8, 64,
+    256, 512} over a 2048-slot pool, then the 8192-token chunked prefill.  Each point prints one
+    JSON line: the whole step through gdn_mixed_batch (L2 flushed between steps) and the
+    roofline kernel alone."""
+    import gated_deltanet_linear_spec_gb300 as gdn
+    from gated_deltanet_linear_spec_gb300 import workloads as W
+    from gated_deltanet_linear_spec_gb300.device_batch import to_device
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    hbm, bf16 = peaks.get("hbm_gbs") or FALLBACK_HBM_GBS, peaks.get("bf16_tflops") or FALLBACK_BF16_TFLOPS
+    points = [(d, b) for d in (1, 2, 4) for b in (1, 8, 64, 256, 512)] + [("prefill", 8192)]
+    for d, b in points:
+        if d == "prefill":
+            batch = W.long_prefill(b)
+            name = f"long_prefill: one {b}-token chunked-prefill row, same layer"
+        else:
+            batch = W.sweep_point(d, b, seed=4 + d * 10 + b)
+            name = f"sweep: spec verify, {d} drafts ({d + 1} tokens/row), batch {b}, 2048-slot pool"
+        db = to_device(batch)
+        alg = algorithmic_bytes(batch)
+        steps = max(3, min(args.steps, 400 if d != "prefill" else 20))
+        for _ in range(args.warmup):
+            db.run()
+            flush.zero_()
+        torch.cuda.synchronize()
+        ms = statistics.mean(timed(db.run, steps, flush, stream))
+        rows = db.spec if db.spec is not None else db.non_spec
+        y = torch.empty((rows.num_tokens, batch.layer.channels), dtype=torch.float32, device="cuda")
+        gdn.gdn_conv_update(db.layer, db.params, db.pools, db.x, rows, y, db.status)
+        if d == "prefill":
+            ws = torch.empty(gdn.gdn_prefill_workspace_bytes(db.layer, rows, rows.num_seqs), dtype=torch.uint8,
+                             device="cuda")
+            k_ms = statistics.mean(timed(lambda: gdn.gdn_chunk_prefill(db.layer, db.params, db.pools, y, db.a, db.b,
+                                                                       rows, db.out, ws, status=db.status),
+                                         steps, flush, stream))
+            roof = {"kernel": "gdn_chunk_prefill", "bound": "tensor", "unit": "TFLOP/s", "peak": bf16,
+                    "achieved": prefill_flops(batch) / (k_ms * 1e-3) / 1e12, "launch_ms": k_ms}
+        else:
+            k_ms = statistics.mean(timed(lambda: gdn.gdn_recurrent_step(db.layer, db.params, db.pools, y, db.a, db.b,
+                                                                        rows, db.out, db.status),
+                                         steps, flush, stream))
+            roof = {"kernel": "gdn::recurrent_kernel", "bound": "hbm", "unit": "GB/s", "peak": hbm,
+                    "achieved": alg["recurrence"] / (k_ms * 1e-3) / 1e9, "launch_ms": k_ms,
+                    "algorithmic_bytes_per_launch": alg["recurrence"]}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        T = batch.num_actual_tokens
+        line = {"metric": METRIC, "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "sweep": True,
+                "config": {"workload": name, "tokens_per_step": T, "l2": "flushed between steps",
+                           "hbm_gbs_whole_step": alg["total"] / (ms * 1e-3) / 1e9, "status": int(db.status.item())},
+                "roofline": roof}
+        print(json.dumps(line), flush=True)
+        del db, y
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -259,8 +320,12 @@ def main() -> int:
     ap.add_argument("--conv-layout", default="rolled", choices=["rolled", "per_slot"],
                     help="spec conv history: rolled at column 0, or one snapshot per spec slot")
     ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of the step")
+    ap.add_argument("--sweep", action="store_true",
+                    help="one line per point of the throughput sweep (drafts x batch, and the long prefill)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.sweep:
+        return run_sweep(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
