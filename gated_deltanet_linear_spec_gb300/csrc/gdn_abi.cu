@@ -266,7 +266,7 @@ int gdn_chunk_prefill(const gdn_layer_desc* layer, const gdn_layer_params* param
   if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16) return GDN_ERR_DTYPE;
   if (rows->num_seqs == 0) return GDN_OK;
   if (!qkv || !a || !b || !out) return GDN_ERR_NULL_ARG;
-  if (!aligned16(qkv)) return GDN_ERR_ALIGN;
+  if (!aligned16(qkv) || !aligned16(out)) return GDN_ERR_ALIGN;  // the scan writes 16-byte output vectors
   if (num_global_tokens < 0) return GDN_ERR_SHAPE;
   if (!rows->token_indx && rows->num_tokens > num_global_tokens) return GDN_ERR_SHAPE;
   const size_t need = gdn_prefill_workspace_bytes(layer, rows, rows->num_seqs);
@@ -299,6 +299,7 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
   if (!aligned16(x)) return GDN_ERR_ALIGN;
   // prefill rows take the tensor-core chunked path when the layer allows it
   const bool chunked = num_prefills > 0 && prefill_tc_supported(layer);
+  if (chunked && !aligned16(out)) return GDN_ERR_ALIGN;  // the scan writes 16-byte output vectors
   const size_t base = gdn_workspace_bytes(layer, non_spec, spec);
   const size_t need = base + (chunked ? gdn_prefill_workspace_bytes(layer, non_spec, num_prefills) : 0);
   if (need && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;

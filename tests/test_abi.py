@@ -72,7 +72,7 @@ def ns_rows(n=8, t=8, **kw):
 
 
 def mixed(lib, layer=None, prm=None, pl=None, non_spec=None, spec=None, n_tokens=None, decodes=8, prefills=0,
-          x=FAKE, ws=FAKE, ws_bytes=1 << 40, a=FAKE):
+          x=FAKE, ws=FAKE, ws_bytes=1 << 40, a=FAKE, out=FAKE):
     layer = layer or big_layer()
     prm = prm or params()
     pl = pl or pools()
@@ -81,7 +81,7 @@ def mixed(lib, layer=None, prm=None, pl=None, non_spec=None, spec=None, n_tokens
     if n_tokens is None:
         n_tokens = spec.num_tokens + non_spec.num_tokens
     return lib.gdn_mixed_batch(ctypes.byref(layer), ctypes.byref(prm), ctypes.byref(pl), x, a, FAKE, n_tokens,
-                               ctypes.byref(non_spec), decodes, prefills, ctypes.byref(spec), FAKE, ws, ws_bytes,
+                               ctypes.byref(non_spec), decodes, prefills, ctypes.byref(spec), out, ws, ws_bytes,
                                None, None)
 
 
@@ -218,3 +218,9 @@ def test_static_workspace_rejects_large_batches_before_touching_the_gpu(lib):
                                               FAKE, FAKE, s.num_tokens, None, 0, 0, ctypes.byref(s), FAKE, None,
                                               None)
     assert rc == ERR["WORKSPACE"]
+
+
+def test_output_alignment_on_the_chunked_path(lib):
+    # the tensor-core prefill writes 16-byte output vectors: a misaligned out is refused there
+    pre = ns_rows(n=8, t=300)
+    assert mixed(lib, non_spec=pre, decodes=6, prefills=2, out=FAKE + 2) == ERR["ALIGN"]
