@@ -62,64 +62,12 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
   if (c0 >= p.C) return;
   const bool reporter = (c0 == 0);
 
+  // Loads that do not depend on one another go out together: the row's token range, its
+  // acceptance, its own (or column-0) slot, and the thread's weights.
   const int32_t bos = __ldg(R.qsl + n), eos = __ldg(R.qsl + n + 1);
-  if (bos < 0 || eos < bos || eos > R.num_tokens) {
-    if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
-    return;
-  }
-  const int L = eos - bos;
-  if (L == 0) return;
-  if (R.is_spec && L > R.spec_cols) {
-    if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
-    return;
-  }
-  const int t0 = seg * kConvSeg;
-  if (t0 >= L) return;
-  const int t1 = min(L, t0 + kConvSeg);
-
-  int slot, anchor;  // the row's conv slot; the history's column offset
-  int rd;            // the slot the history is read from
-  bool read_prior;
-  const bool per_slot = R.is_spec && p.conv_layout == GDN_CONV_PER_SLOT;
-  if (R.is_spec) {
-    const int na = __ldg(R.num_acc + n);
-    if (na < 1 || na > R.spec_cols) {
-      if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
-      return;
-    }
-    // rolled: the history sits in column 0's slot at offset na-1; per slot: it is the snapshot
-    // taken after the last accepted token
-    slot = rd = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + (per_slot ? na - 1 : 0));
-    anchor = per_slot ? 0 : na - 1;
-    read_prior = rd > 0;
-  } else {
-    slot = rd = __ldg(R.state_idx + n);
-    anchor = 0;
-    if (R.num_acc) {
-      // acceptance-aware row: the history its previous verify step accepted
-      const int na = __ldg(R.num_acc + n);
-      if (na < 1 || na > R.spec_cols) {
-        if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
-        return;
-      }
-      if (p.conv_layout == GDN_CONV_PER_SLOT) rd = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1);
-      else anchor = na - 1;
-    }
-    read_prior = rd > 0 && (R.has_init == nullptr || __ldg(R.has_init + n) != 0);
-  }
-  if (slot >= p.num_slots || rd >= p.num_slots) {
-    if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
-    if (slot >= p.num_slots) slot = 0;
-    read_prior = false;
-  }
-
-  const T* __restrict__ x = static_cast<const T*>(p.x);
-  const int64_t xc = x_channel(p, c0);  // where this thread's 8 channels sit in a row of x
-  T* __restrict__ pool = static_cast<T*>(p.conv_pool);
-  const int64_t C = p.C;
-  const int64_t slot_base = (int64_t)slot * p.state_len * C + c0;
-  const int64_t hist_base = (int64_t)(read_prior ? rd : 0) * p.state_len * C + c0;
-
+  const int na = R.num_acc ? __ldg(R.num_acc + n) : 1;
+  const int own = R.is_spec ? __ldg(R.spec_idx + (int64_t)n * R.spec_cols) : __ldg(R.state_idx + n);
+  const bool has_init = R.is_spec || R.has_init == nullptr || __ldg(R.has_init + n) != 0;
   // Weights and bias of the thread's 8 channels: 8*W contiguous elements, 16-byte vectors.
   float w[W][8], bias[8];
   {
@@ -143,6 +91,56 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
 #pragma unroll
     for (int e = 0; e < 8; ++e) bias[e] = 0.f;
   }
+
+  if (bos < 0 || eos < bos || eos > R.num_tokens) {
+    if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
+    return;
+  }
+  const int L = eos - bos;
+  if (L == 0) return;
+  if (R.is_spec && L > R.spec_cols) {
+    if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
+    return;
+  }
+  const int t0 = seg * kConvSeg;
+  if (t0 >= L) return;
+  const int t1 = min(L, t0 + kConvSeg);
+
+  int slot, anchor;  // the row's conv slot; the history's column offset
+  int rd;            // the slot the history is read from
+  bool read_prior;
+  const bool per_slot = R.is_spec && p.conv_layout == GDN_CONV_PER_SLOT;
+  if (R.num_acc && (na < 1 || na > R.spec_cols)) {
+    if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
+    return;
+  }
+  if (R.is_spec) {
+    // rolled: the history sits in column 0's slot at offset na-1; per slot: it is the snapshot
+    // taken after the last accepted token
+    slot = rd = per_slot ? __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1) : own;
+    anchor = per_slot ? 0 : na - 1;
+    read_prior = rd > 0;
+  } else {
+    slot = rd = own;
+    anchor = 0;
+    if (R.num_acc) {  // acceptance-aware row: the history its previous verify step accepted
+      if (p.conv_layout == GDN_CONV_PER_SLOT) rd = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + na - 1);
+      else anchor = na - 1;
+    }
+    read_prior = rd > 0 && has_init;
+  }
+  if (slot >= p.num_slots || rd >= p.num_slots) {
+    if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
+    if (slot >= p.num_slots) slot = 0;
+    read_prior = false;
+  }
+
+  const T* __restrict__ x = static_cast<const T*>(p.x);
+  const int64_t xc = x_channel(p, c0);  // where this thread's 8 channels sit in a row of x
+  T* __restrict__ pool = static_cast<T*>(p.conv_pool);
+  const int64_t C = p.C;
+  const int64_t slot_base = (int64_t)slot * p.state_len * C + c0;
+  const int64_t hist_base = (int64_t)(read_prior ? rd : 0) * p.state_len * C + c0;
 
   // Raw window of the W-1 inputs before the current token: the slot's history (segment 0)
   // or the row's previous inputs (later segments).
