@@ -199,9 +199,32 @@ def oracle_tokens_per_s(batch, budget_s: float = 12.0, heads=None) -> dict:
         el += time.perf_counter() - t0
         reps += 1
     what = "all 32 v-heads" if heads is None else f"v-heads {heads[0]}..{heads[1] - 1} of {Hv}, scaled to all"
+    # one single-thread pass of the same sample, for the per-core rate
+    t0 = time.perf_counter()
+    run_oracle(batch, heads=heads, nthreads=1, conv_pool=conv_pool, ssm_pool=ssm_pool)
+    one = time.perf_counter() - t0
     return {"value": reps * batch.num_actual_tokens * frac / el, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"the full token set ({batch.num_actual_tokens} tokens), {what}, repeated {reps}x: "
-                      f"{el:.1f} s of CPU time on {cores} threads"}
+                      f"{el:.1f} s of CPU time on {cores} threads",
+            "single_thread_value": batch.num_actual_tokens * frac / one, "cpu_model": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name, as the kernel reports it (empty when it does not)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip().lower() in ("model name", "cpu model"):
+                    return v.strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip().lower() == "model name":
+                return v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return ""
 
 
 # ------------------------------------------------------------------------------------------

@@ -134,3 +134,28 @@ def test_per_slot_chain_matches_rolled_chain(layer):
     for n in range(n_rows):
         for t in range(k):
             assert np.array_equal(rs2.conv_pool[ssi[n, t], :W - 1], rr2.conv_pool[ssi[n, 0], t: t + W - 1])
+
+
+def test_negative_control_scattered_snapshots_are_not_the_rolled_contract():
+    # "[GDN] Spec-decoding-aware attention kernel", Problem: under the rolled contract only the
+    # column-0 slot of a verify row is updated and columns 1..K-1 stay untouched; writing
+    # per-token snapshots across the K slots and then reading the ring as rolled diverges.
+    layer, k = SMALL, 4
+    rows = [RowSpec("spec", k, 1 + i % k) for i in range(5)]
+    b1 = build_batch(layer, rows, num_slots=48, spec_cols=k, seed=61)
+    pre = _raw(b1.conv_pool)
+    rolled = run_oracle(b1)
+    scattered = run_oracle(with_layouts(b1, conv_layout=1))
+    ssi = b1.spec.spec_state_indices.numpy()
+    for n in range(len(rows)):
+        for t in range(1, k):
+            assert np.array_equal(rolled.conv_pool[ssi[n, t]], pre[ssi[n, t]])       # untouched
+        assert not np.array_equal(scattered.conv_pool[ssi[n, k - 1]], pre[ssi[n, k - 1]])  # written
+    # the next verify step reads the ring as rolled: from the scattered pool its outputs differ
+    b2 = build_batch(layer, [RowSpec("spec", k, 3) for _ in range(5)], num_slots=48, spec_cols=k, seed=62)
+    b2.spec = copy.copy(b2.spec)
+    b2.spec.spec_state_indices = b1.spec.spec_state_indices.clone()
+    good = run_oracle(b2, conv_pool=rolled.conv_pool.copy(), ssm_pool=rolled.ssm_pool.copy())
+    bad = run_oracle(b2, conv_pool=scattered.conv_pool.copy(), ssm_pool=scattered.ssm_pool.copy())
+    diff = np.abs(good.out_f64 - bad.out_f64).max()
+    assert diff > 1e-3, diff
