@@ -629,12 +629,13 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     }
     ++mma_commits[0];
     if (c > 0) store_outputs(c - 1);  // while the U products run
-    ok = __syncthreads_and(tc::mbar_wait(&bar_mma[0], mma_done[0] & 1));
+    // Each warp goes on as soon as U is ready (the issuing thread's warp joins after issuing the
+    // output products); the block-wide barrier comes only before the next products are issued.
+    const bool u_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[0], mma_done[0] & 1));
     ++mma_done[0];
-    if (!ok) break;
-    tc::fence_after();
     // U += U~; U^T images (row = dv, column = t)
-    {
+    if (u_ok) {
+      tc::fence_after();
       float u[32];
       tc::tmem_ld32(tc::tmem_lane_col(tU, warp, 0), u);
       if (lane < 16) {
@@ -651,7 +652,8 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     }
     tc::fence_async_smem();
     tc::fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(u_ok);
+    if (!ok) break;
     // S^T += K'^T U (three passes) -> commit;  O += P U -> commit
     if (tid == 0) {
       tc::fence_after();
@@ -671,28 +673,29 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     }
     ++mma_commits[1];
     ++mma_commits[2];
-    ok = __syncthreads_and(tc::mbar_wait(&bar_mma[1], mma_done[1] & 1));
+    const bool s_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[1], mma_done[1] & 1));
     ++mma_done[1];
-    if (!ok) break;
-    tc::fence_after();
-    // the new state: images for the next chunk, then gamma_{c+1} S^T back into TMEM
-    tc::tmem_ld32(tc::tmem_lane_col(tS, warp, 0), v);
     bool tma_ok = true;
-    if (c + 1 < nch) {
+    if (s_ok) {
+      tc::fence_after();
+      // the new state: images for the next chunk, then gamma_{c+1} S^T back into TMEM
+      tc::tmem_ld32(tc::tmem_lane_col(tS, warp, 0), v);
+      if (c + 1 < nch) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) put_pair(s_hi, s_lo, tc::img_off(j, dk, 2), v[j]);
-      const int nb = (c + 1) & 1;
-      tma_ok = tc::mbar_wait(&bar_tma[nb], tma_done[nb] & 1);
-      ++tma_done[nb];
-      const float gn = *reinterpret_cast<const float*>(sm + nb * kBufBytes + kBufMeta);
+        for (int j = 0; j < 32; ++j) put_pair(s_hi, s_lo, tc::img_off(j, dk, 2), v[j]);
+        const int nb = (c + 1) & 1;
+        tma_ok = tc::mbar_wait(&bar_tma[nb], tma_done[nb] & 1);
+        ++tma_done[nb];
+        const float gn = *reinterpret_cast<const float*>(sm + nb * kBufBytes + kBufMeta);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= gn;
-      tc::tmem_st32(tc::tmem_lane_col(tS, warp, 0), v);
-    } else if (slot > 0) {
+        for (int j = 0; j < 32; ++j) v[j] *= gn;
+        tc::tmem_st32(tc::tmem_lane_col(tS, warp, 0), v);
+      } else if (slot > 0) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) gS[(int64_t)j * kD] = v[j];
+        for (int j = 0; j < 32; ++j) gS[(int64_t)j * kD] = v[j];
+      }
     }
-    const bool mma_ok = tc::mbar_wait(&bar_mma[2], mma_done[2] & 1);
+    const bool mma_ok = s_ok && tc::mbar_wait(&bar_mma[2], mma_done[2] & 1);
     ok = __syncthreads_and(tma_ok && mma_ok);
     ++mma_done[2];
     if (!ok) break;
