@@ -512,8 +512,10 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   uint8_t* u_hi = sm + kUImg;
   uint8_t* u_lo = u_hi + 4096;
   // one barrier per commit point, each committed and waited once per chunk (so a wait is never
-  // more than one phase behind): U ready; state update (and the first O half) done; O done
-  __shared__ __align__(8) uint64_t bar_mma[3], bar_tma[2];
+  // more than one phase behind): U ready; state update done; O done; the first O half done.
+  // Thread 0 issues the U and state products, thread 32 the output products, so neither
+  // stream of MMAs waits behind the other's issue.
+  __shared__ __align__(8) uint64_t bar_mma[4], bar_tma[2];
   __shared__ uint32_t tmem_base;
   __shared__ int sGt[2][kCh];  // global tokens of the chunk whose outputs are pending
 
@@ -546,7 +548,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
 
   if (warp == 0) tc::tmem_alloc(&tmem_base, 128);
   if (tid == 32) {
-    for (int i = 0; i < 3; ++i) tc::mbar_init(&bar_mma[i], 1);
+    for (int i = 0; i < 4; ++i) tc::mbar_init(&bar_mma[i], 1);
     tc::mbar_init(&bar_tma[0], 1);
     tc::mbar_init(&bar_tma[1], 1);
     tc::mbar_init_fence();
@@ -582,7 +584,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     if (nch > 1) issue(1);
   }
   int tma_issued[2] = {1, nch > 1 ? 1 : 0}, tma_done[2] = {0, 0};
-  int mma_commits[3] = {0, 0, 0}, mma_done[3] = {0, 0, 0};
+  int mma_commits[4] = {0, 0, 0, 0}, mma_done[4] = {0, 0, 0, 0};
 
   // initial state: images of S_0 (unscaled) and gamma_0 S_0^T in TMEM
   float v[32];
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
       sGt[b][tid] = t < L ? global_token(p.rows, bos + t, p.num_global, p.status) : -1;
     }
     const uint32_t tO = tO0 + 32 * b;
-    // U = -W S_0^T (three passes) -> commit;  O = (gamma q^) S_0^T
+    // U = -W S_0^T (three passes) -> commit (thread 0);  O = (gamma q^) S_0^T -> commit (thread 32)
     if (tid == 0) {
       tc::fence_after();
       const uint32_t id = tc::idesc_bf16(64, 32);
@@ -622,12 +624,18 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
                  tc::sdesc(sl + off, 2048), id, s == 0);
       }
       tc::commit(&bar_mma[0]);
+    } else if (tid == 32) {
+      tc::fence_after();
+      const uint32_t id = tc::idesc_bf16(64, 32);
+      const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi);
       for (int s = 0; s < 8; ++s) {
         const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
         tc::mma(tO, tc::sdesc(bb + kQp + off, 2048), tc::sdesc(sh + off, 2048), id, s > 0 ? 1u : 0u);
       }
+      tc::commit(&bar_mma[3]);
     }
     ++mma_commits[0];
+    ++mma_commits[3];
     if (c > 0) store_outputs(c - 1);  // while the U products run
     // Each warp goes on as soon as U is ready (the issuing thread's warp joins after issuing the
     // output products); the block-wide barrier comes only before the next products are issued.
@@ -654,10 +662,10 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     tc::fence_before();
     ok = __syncthreads_and(u_ok);
     if (!ok) break;
-    // S^T += K'^T U (three passes) -> commit;  O += P U -> commit
+    // S^T += K'^T U (three passes) -> commit (thread 0);  O += P U -> commit (thread 32)
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t id64 = tc::idesc_bf16(64, 32), id128 = tc::idesc_bf16(128, 32);
+      const uint32_t id128 = tc::idesc_bf16(128, 32);
       const uint32_t bb = tc::smem_addr(buf), uh = tc::smem_addr(u_hi), ul = tc::smem_addr(u_lo);
       for (int s = 0; s < 4; ++s) {
         const uint32_t off = s * 32;
@@ -665,6 +673,10 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
                  tc::sdesc(ul + off, 1024), id128, false);
       }
       tc::commit(&bar_mma[1]);
+    } else if (tid == 32) {  // after its own first half, in issue order on this thread
+      tc::fence_after();
+      const uint32_t id64 = tc::idesc_bf16(64, 32);
+      const uint32_t bb = tc::smem_addr(buf), uh = tc::smem_addr(u_hi);
       for (int s = 0; s < 4; ++s) {
         const uint32_t off = s * 32;
         tc::mma(tO, tc::sdesc(bb + kP + off, 1024), tc::sdesc(uh + off, 1024), id64, 1u);
@@ -673,8 +685,12 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     }
     ++mma_commits[1];
     ++mma_commits[2];
-    const bool s_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[1], mma_done[1] & 1));
+    // the state images are rewritten below: the state products and the first output half (which
+    // read them) must be done
+    const bool s_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[1], mma_done[1] & 1) &&
+                                                  tc::mbar_wait(&bar_mma[3], mma_done[3] & 1));
     ++mma_done[1];
+    ++mma_done[3];
     bool tma_ok = true;
     if (s_ok) {
       tc::fence_after();
@@ -715,7 +731,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     if (tid == 0) set_status(p.status, GDN_STATUS_WAIT_TIMEOUT);
     // bounded drains of anything still in flight (the wait that failed included) before TMEM
     // and shared memory are released
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 4; ++i)
       for (int k = mma_done[i] > 0 ? mma_done[i] - 1 : 0; k < mma_commits[i]; ++k) tc::mbar_wait(&bar_mma[i], k & 1);
     for (int bb = 0; bb < 2; ++bb)
       for (int k = tma_done[bb] > 0 ? tma_done[bb] - 1 : 0; k < tma_issued[bb]; ++k) tc::mbar_wait(&bar_tma[bb], k & 1);
