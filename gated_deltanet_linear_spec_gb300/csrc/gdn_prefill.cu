@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   // more than one phase behind): U ready; state update done; O done; the first O half done.
   // Thread 0 issues the U and state products, thread 32 the output products, so neither
   // stream of MMAs waits behind the other's issue.
-  __shared__ __align__(8) uint64_t bar_mma[4], bar_tma[2];
+  __shared__ __align__(8) uint64_t bar_mma[5], bar_tma[2];
   __shared__ uint32_t tmem_base;
   __shared__ int sGt[2][kCh];  // global tokens of the chunk whose outputs are pending
 
@@ -546,9 +546,9 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   const float* gS0 = p.ssm_pool + ((int64_t)(read_prior ? load_slot : 0) * p.Hv + h) * kD * kD + (int64_t)dv0 * kD + dk;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 
-  if (warp == 0) tc::tmem_alloc(&tmem_base, 128);
+  if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
   if (tid == 32) {
-    for (int i = 0; i < 4; ++i) tc::mbar_init(&bar_mma[i], 1);
+    for (int i = 0; i < 5; ++i) tc::mbar_init(&bar_mma[i], 1);
     tc::mbar_init(&bar_tma[0], 1);
     tc::mbar_init(&bar_tma[1], 1);
     tc::mbar_init_fence();
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   __syncthreads();
   tc::fence_after();
   // O alternates between two accumulators: chunk c's outputs are drained while chunk c + 1 runs
-  const uint32_t tS = tmem_base, tU = tmem_base + 32, tO0 = tmem_base + 64;
+  const uint32_t tS = tmem_base, tU = tmem_base + 32, tO0 = tmem_base + 64, tU2 = tmem_base + 128;
   auto store_outputs = [&](int c) {  // row t of O -> 32 bf16 of out[token][h][dv0 ..]
     float o[32];
     tc::tmem_ld32(tc::tmem_lane_col(tO0 + 32 * (c & 1), warp, 0), o);
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     if (nch > 1) issue(1);
   }
   int tma_issued[2] = {1, nch > 1 ? 1 : 0}, tma_done[2] = {0, 0};
-  int mma_commits[4] = {0, 0, 0, 0}, mma_done[4] = {0, 0, 0, 0};
+  int mma_commits[5] = {0, 0, 0, 0, 0}, mma_done[5] = {0, 0, 0, 0, 0};
 
   // initial state: images of S_0 (unscaled) and gamma_0 S_0^T in TMEM
   float v[32];
@@ -618,12 +618,22 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
       tc::fence_after();
       const uint32_t id = tc::idesc_bf16(64, 32);
       const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi), sl = tc::smem_addr(s_lo);
-      for (int s = 0; s < 8; ++s) {
+      for (int s = 0; s < 4; ++s) {  // first half of K into tU, the second half on thread 64
         const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
         tc::mma3(tU, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc(sh + off, 2048),
                  tc::sdesc(sl + off, 2048), id, s == 0);
       }
       tc::commit(&bar_mma[0]);
+    } else if (tid == 64) {
+      tc::fence_after();
+      const uint32_t id = tc::idesc_bf16(64, 32);
+      const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi), sl = tc::smem_addr(s_lo);
+      for (int s = 4; s < 8; ++s) {
+        const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
+        tc::mma3(tU2, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc(sh + off, 2048),
+                 tc::sdesc(sl + off, 2048), id, s == 4);
+      }
+      tc::commit(&bar_mma[4]);
     } else if (tid == 32) {
       tc::fence_after();
       const uint32_t id = tc::idesc_bf16(64, 32);
@@ -636,16 +646,22 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     }
     ++mma_commits[0];
     ++mma_commits[3];
+    ++mma_commits[4];
     if (c > 0) store_outputs(c - 1);  // while the U products run
     // Each warp goes on as soon as U is ready (the issuing thread's warp joins after issuing the
     // output products); the block-wide barrier comes only before the next products are issued.
-    const bool u_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[0], mma_done[0] & 1));
+    const bool u_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[0], mma_done[0] & 1) &&
+                                                  tc::mbar_wait(&bar_mma[4], mma_done[4] & 1));
     ++mma_done[0];
+    ++mma_done[4];
     // U += U~; U^T images (row = dv, column = t)
     if (u_ok) {
       tc::fence_after();
-      float u[32];
+      float u[32], u2[32];
       tc::tmem_ld32(tc::tmem_lane_col(tU, warp, 0), u);
+      tc::tmem_ld32(tc::tmem_lane_col(tU2, warp, 0), u2);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) u[j] += u2[j];
       if (lane < 16) {
         const int t = 16 * warp + lane;
         const float4* ut = reinterpret_cast<const float4*>(buf + kBufUt) + t * 8;
@@ -731,14 +747,14 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     if (tid == 0) set_status(p.status, GDN_STATUS_WAIT_TIMEOUT);
     // bounded drains of anything still in flight (the wait that failed included) before TMEM
     // and shared memory are released
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 5; ++i)
       for (int k = mma_done[i] > 0 ? mma_done[i] - 1 : 0; k < mma_commits[i]; ++k) tc::mbar_wait(&bar_mma[i], k & 1);
     for (int bb = 0; bb < 2; ++bb)
       for (int k = tma_done[bb] > 0 ? tma_done[bb] - 1 : 0; k < tma_issued[bb]; ++k) tc::mbar_wait(&bar_tma[bb], k & 1);
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem_base, 128);
+  if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
 }
 
 template <typename QT>
