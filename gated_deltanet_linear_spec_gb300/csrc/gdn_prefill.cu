@@ -662,17 +662,22 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
       tc::tmem_ld32(tc::tmem_lane_col(tU2, warp, 0), u2);
 #pragma unroll
       for (int j = 0; j < 32; ++j) u[j] += u2[j];
-      if (lane < 16) {
-        const int t = 16 * warp + lane;
-        const float4* ut = reinterpret_cast<const float4*>(buf + kBufUt) + t * 8;
+      // rows t of this warp sit in lanes 0..15; lanes 16..31 take over columns 16..31 of them
+      const int half = lane >> 4, t = 16 * warp + (lane & 15);
+      float w16[16];
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 f = ut[j4];
-          u[4 * j4] += f.x; u[4 * j4 + 1] += f.y; u[4 * j4 + 2] += f.z; u[4 * j4 + 3] += f.w;
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) put_pair(u_hi, u_lo, tc::img_off(j, t, 1), u[j]);
+      for (int j = 0; j < 16; ++j) {
+        const float hi_half = __shfl_sync(0xffffffffu, u[16 + j], lane & 15);
+        w16[j] = half ? hi_half : u[j];
       }
+      const float4* ut = reinterpret_cast<const float4*>(buf + kBufUt) + t * 8 + 4 * half;
+#pragma unroll
+      for (int j4 = 0; j4 < 4; ++j4) {
+        const float4 f = ut[j4];
+        w16[4 * j4] += f.x; w16[4 * j4 + 1] += f.y; w16[4 * j4 + 2] += f.z; w16[4 * j4 + 3] += f.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) put_pair(u_hi, u_lo, tc::img_off(16 * half + j, t, 1), w16[j]);
     }
     tc::fence_async_smem();
     tc::fence_before();
