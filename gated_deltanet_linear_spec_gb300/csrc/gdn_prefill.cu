@@ -590,8 +590,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = read_prior ? gS0[(int64_t)j * kD] : 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) put_pair(s_hi, s_lo, tc::img_off(j, dk, 2), v[j]);
+  tc::put_mn32_row(s_hi, s_lo, dk, v, 0, 4);
   bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma[0], 0));
   tma_done[0] = 1;
   if (ok) {
@@ -616,31 +615,31 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     // U = -W S_0^T (three passes) -> commit (thread 0);  O = (gamma q^) S_0^T -> commit (thread 32)
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t id = tc::idesc_bf16(64, 32);
+      const uint32_t id = tc::idesc_bf16_bmn(64, 32);
       const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi), sl = tc::smem_addr(s_lo);
       for (int s = 0; s < 4; ++s) {  // first half of K into tU, the second half on thread 64
         const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
-        tc::mma3(tU, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc(sh + off, 2048),
-                 tc::sdesc(sl + off, 2048), id, s == 0);
+        tc::mma3(tU, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc_mn32(sh + 1024 * s),
+                 tc::sdesc_mn32(sl + 1024 * s), id, s == 0);
       }
       tc::commit(&bar_mma[0]);
     } else if (tid == 64) {
       tc::fence_after();
-      const uint32_t id = tc::idesc_bf16(64, 32);
+      const uint32_t id = tc::idesc_bf16_bmn(64, 32);
       const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi), sl = tc::smem_addr(s_lo);
       for (int s = 4; s < 8; ++s) {
         const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
-        tc::mma3(tU2, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc(sh + off, 2048),
-                 tc::sdesc(sl + off, 2048), id, s == 4);
+        tc::mma3(tU2, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc_mn32(sh + 1024 * s),
+                 tc::sdesc_mn32(sl + 1024 * s), id, s == 4);
       }
       tc::commit(&bar_mma[4]);
     } else if (tid == 32) {
       tc::fence_after();
-      const uint32_t id = tc::idesc_bf16(64, 32);
+      const uint32_t id = tc::idesc_bf16_bmn(64, 32);
       const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi);
       for (int s = 0; s < 8; ++s) {
         const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
-        tc::mma(tO, tc::sdesc(bb + kQp + off, 2048), tc::sdesc(sh + off, 2048), id, s > 0 ? 1u : 0u);
+        tc::mma(tO, tc::sdesc(bb + kQp + off, 2048), tc::sdesc_mn32(sh + 1024 * s), id, s > 0 ? 1u : 0u);
       }
       tc::commit(&bar_mma[3]);
     }
@@ -676,8 +675,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
         const float4 f = ut[j4];
         w16[4 * j4] += f.x; w16[4 * j4 + 1] += f.y; w16[4 * j4 + 2] += f.z; w16[4 * j4 + 3] += f.w;
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) put_pair(u_hi, u_lo, tc::img_off(16 * half + j, t, 1), w16[j]);
+      tc::put_mn32_row(u_hi, u_lo, t, w16, 2 * half, 2);
     }
     tc::fence_async_smem();
     tc::fence_before();
@@ -686,21 +684,21 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     // S^T += K'^T U (three passes) -> commit (thread 0);  O += P U -> commit (thread 32)
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t id128 = tc::idesc_bf16(128, 32);
+      const uint32_t id128 = tc::idesc_bf16_bmn(128, 32);
       const uint32_t bb = tc::smem_addr(buf), uh = tc::smem_addr(u_hi), ul = tc::smem_addr(u_lo);
       for (int s = 0; s < 4; ++s) {
         const uint32_t off = s * 32;
-        tc::mma3(tS, tc::sdesc(bb + kKpHi + off, 1024), tc::sdesc(bb + kKpLo + off, 1024), tc::sdesc(uh + off, 1024),
-                 tc::sdesc(ul + off, 1024), id128, false);
+        tc::mma3(tS, tc::sdesc(bb + kKpHi + off, 1024), tc::sdesc(bb + kKpLo + off, 1024), tc::sdesc_mn32(uh + 1024 * s),
+                 tc::sdesc_mn32(ul + 1024 * s), id128, false);
       }
       tc::commit(&bar_mma[1]);
     } else if (tid == 32) {  // after its own first half, in issue order on this thread
       tc::fence_after();
-      const uint32_t id64 = tc::idesc_bf16(64, 32);
+      const uint32_t id64 = tc::idesc_bf16_bmn(64, 32);
       const uint32_t bb = tc::smem_addr(buf), uh = tc::smem_addr(u_hi);
       for (int s = 0; s < 4; ++s) {
         const uint32_t off = s * 32;
-        tc::mma(tO, tc::sdesc(bb + kP + off, 1024), tc::sdesc(uh + off, 1024), id64, 1u);
+        tc::mma(tO, tc::sdesc(bb + kP + off, 1024), tc::sdesc_mn32(uh + 1024 * s), id64, 1u);
       }
       tc::commit(&bar_mma[2]);
     }
@@ -718,8 +716,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
       // the new state: images for the next chunk, then gamma_{c+1} S^T back into TMEM
       tc::tmem_ld32(tc::tmem_lane_col(tS, warp, 0), v);
       if (c + 1 < nch) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) put_pair(s_hi, s_lo, tc::img_off(j, dk, 2), v[j]);
+        tc::put_mn32_row(s_hi, s_lo, dk, v, 0, 4);
         const int nb = (c + 1) & 1;
         tma_ok = tc::mbar_wait(&bar_tma[nb], tma_done[nb] & 1);
         ++tma_done[nb];

@@ -9,6 +9,8 @@
 // fp32 values enter the tensor core as a bf16 hi/lo pair (hi = rn(x), lo = rn(x - hi)); a
 // product a*b is formed by three MMAs (hi*hi + hi*lo + lo*hi) into an fp32 accumulator, which
 // keeps about 16 significant bits per operand.
+// B operands with N = 32 may instead be MN-major with the 64-byte swizzle (mn32_off), so a
+// thread holding one k's 32 values writes them as four 16-byte chunks.
 // Accumulators: with M = 128 and one CTA, row m of D is TMEM lane m and column n is TMEM column
 // base + n; warp w of the CTA reads and writes lanes 32*(w%4) .. 32*(w%4)+31.
 #pragma once
@@ -33,10 +35,27 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t group_stride)
          ((uint64_t)((group_stride >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Byte offset of element (n, k) in a bf16 MN-major tile with N = 32 and the 64-byte swizzle:
+// for each k a 64-byte row of the 32 n values; 8 rows (k) form a 512-byte atom, atoms along k
+// packed.  Inside an atom the 16-byte chunk j of row r sits at j ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint32_t mn32_off(int n, int k) {
+  const int r = k & 7;
+  return (uint32_t)((k >> 3) * 512 + r * 64 + ((((n >> 3)) ^ ((r >> 1) & 3)) << 4) + (n & 7) * 2);
+}
+
+// Descriptor of an N = 32 MN-major tile with the 64-byte swizzle (512-byte atoms along K).
+__device__ __forceinline__ uint64_t sdesc_mn32(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+
 // Instruction descriptor: kind::f16, bf16 x bf16 -> fp32, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+
+// The same with the B operand MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
 
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -153,6 +172,19 @@ __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
   }
   hi = *reinterpret_cast<const uint4*>(h);
   lo = *reinterpret_cast<const uint4*>(l);
+}
+// 32 fp32 values of row k of an N = 32 MN-major hi/lo image pair (chunks c0 .. c0+nc-1 of 8).
+__device__ __forceinline__ void put_mn32_row(uint8_t* hi_img, uint8_t* lo_img, int k, const float* x, int c0, int nc) {
+  const int r = k & 7;
+  const uint32_t base = (uint32_t)((k >> 3) * 512 + r * 64);
+#pragma unroll
+  for (int c = c0; c < c0 + nc; ++c) {
+    uint4 hi, lo;
+    split8(x + 8 * (c - c0), hi, lo);
+    const uint32_t off = base + ((uint32_t)(c ^ ((r >> 1) & 3)) << 4);
+    *reinterpret_cast<uint4*>(hi_img + off) = hi;
+    *reinterpret_cast<uint4*>(lo_img + off) = lo;
+  }
 }
 __device__ __forceinline__ uint4 pack8(const float* x) {
   __nv_bfloat16 h[8];
