@@ -41,7 +41,7 @@ constexpr int kD = 128;             // dk = dv on this path
 // Per (chunk, v-head) record written by the prep kernel, read by the scan kernel.
 constexpr uint32_t kWnHi = 0;       // -W   [t][dk]  bf16 hi image (K-major, 2 atoms)   16 KiB
 constexpr uint32_t kWnLo = 16384;   //               bf16 lo image                       16 KiB
-constexpr uint32_t kKpHi = 32768;   // K'^T [dk][s]  bf16 hi image (1 atom)               16 KiB
+constexpr uint32_t kKpHi = 32768;   // K'   [s][dk]  bf16 hi image (2 atoms; read MN-major) 16 KiB
 constexpr uint32_t kKpLo = 49152;   //               bf16 lo image                       16 KiB
 constexpr uint32_t kQp = 65536;     // gamma q^ [t][dk] bf16 image                       16 KiB
 constexpr uint32_t kP = 81920;      // P    [t][s]   bf16 image                           8 KiB
@@ -88,14 +88,6 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
   x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
 }
 
-// One fp32 value as a bf16 hi/lo pair at byte offset off of two images.
-__device__ __forceinline__ void put_pair(uint8_t* hi_img, uint8_t* lo_img, uint32_t off, float x) {
-  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-  *reinterpret_cast<__nv_bfloat16*>(hi_img + off) = hi;
-  *reinterpret_cast<__nv_bfloat16*>(lo_img + off) = lo;
-}
-
 __device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
   const float x = a + dt_bias;
   return -expf(A_log) * (x > 20.f ? x : log1pf(expf(x)));
@@ -107,16 +99,12 @@ template <typename QT>
 __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) {
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* sm = align1k(dyn_smem);
-  uint8_t* qk_hi = sm;  // [q^; k^] [128][128] images (MMA 1)
+  uint8_t* qk_hi = sm;  // [q^; k^] [128][128] images (MMA 1); then [beta v; beta gamma k^] rows (MMA 2, 3)
   uint8_t* qk_lo = sm + 32768;
   float* sA = reinterpret_cast<float*>(sm + 81920);  // A [64][kAStride]  (after MMA 1)
-  uint8_t* kb_hi = sm;  // (beta gamma k^)^T [128][64]  (after MMA 1)
-  uint8_t* kb_lo = sm + 16384;
-  uint8_t* vb_hi = sm + 32768;  // (beta v)^T [128][64]
-  uint8_t* vb_lo = sm + 49152;
   uint8_t* t_hi = sm + 65536;  // T [64][64]
   uint8_t* t_lo = sm + 73728;
-  __shared__ float sG[kCh], sBeta[kCh], sRk[kCh], sFk[kCh], sFp[kCh];
+  __shared__ float sG[kCh], sBeta[kCh], sRk[kCh], sBG[kCh];
   __shared__ float sMs[2][256];  // per-warp 16 x 16 scratch of the blocked solve
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tmem_base;
@@ -232,11 +220,7 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
     }
     tc::commit(&bar);
   }
-  if (tid < kCh) {  // per-token factors of the k^T images: beta gamma / |k| and e^{G_c - G_s} / |k|
-    const float Gc = sG[kCh - 1];
-    sFk[tid] = sBeta[tid] * expf(sG[tid]) * sRk[tid];
-    sFp[tid] = tid < nc ? expf(Gc - sG[tid]) * sRk[tid] : 0.f;
-  }
+  if (tid < kCh) sBG[tid] = sBeta[tid] * expf(sG[tid]);  // beta_t gamma_t, the row scale of k^ in W
   bool ok = __syncthreads_and(tc::mbar_wait(&bar, 0));
   if (ok) {
     tc::fence_after();
@@ -375,51 +359,58 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
         }
       }
     } else {
-      // 6b. meanwhile: (beta gamma k^)^T and (beta v)^T images (shared memory) and the K'^T
-      //     record images, rows d and d + 64 of the thread; the loads of 16 tokens of both rows
-      //     are issued together
+      // 6b. meanwhile: the A operands of MMA 2 and 3, both read MN-major (a [s][d] tile laid out
+      //     like a K-major one): the k^ rows of the [q^; k^] images scaled in place by
+      //     beta_s gamma_s, and the rows beta_s v_s in the q^ half, which MMA 1 no longer needs;
+      //     on the way, the record's K' rows e^{G_c - G_s} k^_s (the same image layout).
       const float Gc = sG[kCh - 1];
-      const int d = tid - 64;
+      for (int i = tid - 64; i < kCh * (kD / 8); i += 64) {
+        const int t = i / (kD / 8), d0 = 8 * (i % (kD / 8));
+        const uint32_t off = tc::img_off(kCh + t, d0, 2);
+        const uint4 h = *reinterpret_cast<const uint4*>(qk_hi + off), l = *reinterpret_cast<const uint4*>(qk_lo + off);
+        const __nv_bfloat16* hb = reinterpret_cast<const __nv_bfloat16*>(&h);
+        const __nv_bfloat16* lb = reinterpret_cast<const __nv_bfloat16*>(&l);
+        float kn[8], x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kn[e] = __bfloat162float(hb[e]) + __bfloat162float(lb[e]);
+        const float f = sBG[t], fp = expf(Gc - sG[t]);  // padded tokens: k^ = 0
+        uint4 nh, nl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = fp * kn[e];
+        tc::split8(x, nh, nl);
+        const uint32_t roff = tc::img_off(t, d0, 2);
+        *reinterpret_cast<uint4*>(rec + kKpHi + roff) = nh;
+        *reinterpret_cast<uint4*>(rec + kKpLo + roff) = nl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = f * kn[e];
+        tc::split8(x, nh, nl);
+        *reinterpret_cast<uint4*>(qk_hi + off) = nh;
+        *reinterpret_cast<uint4*>(qk_lo + off) = nl;
+      }
+      // v rows: warp 2 takes tokens 0..31, warp 3 tokens 32..63, sixteen at a time; lane = 4 dv
+      const int tw0 = (warp - 2) * 32;
 #pragma unroll 1
-      for (int s0 = 0; s0 < kCh; s0 += 16) {
-        float kr[2][16], vr[2][16];
+      for (int i0 = 0; i0 < 32; i0 += 16) {
+        float v[16][4];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int s = s0 + e;
+        for (int u = 0; u < 16; ++u) {
+          const int t = tw0 + i0 + u;
+          if (t < nc) {
+            load4(qkv + (int64_t)(bos + t0 + t) * C + voff + 4 * lane, v[u]);
+          } else {
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            kr[r][e] = vr[r][e] = 0.f;
-            if (s < nc) {
-              const QT* row = qkv + (int64_t)(bos + t0 + s) * C;
-              kr[r][e] = to_f32(row[koff + d + 64 * r]);
-              vr[r][e] = to_f32(row[voff + d + 64 * r]);
-            }
+            for (int e = 0; e < 4; ++e) v[u][e] = 0.f;
           }
         }
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+        for (int u = 0; u < 16; ++u) {
+          const int t = tw0 + i0 + u;
+          const float bs = sBeta[t];
+          float x[4];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float xk[8], xv[8], xp[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int s = s0 + 8 * half + e;
-              xk[e] = sFk[s] * kr[r][8 * half + e];
-              xv[e] = sBeta[s] * vr[r][8 * half + e];
-              xp[e] = sFp[s] * kr[r][8 * half + e];
-            }
-            uint4 hi, lo;
-            const uint32_t off = tc::img_off(d + 64 * r, s0 + 8 * half, 1);
-            tc::split8(xk, hi, lo);
-            *reinterpret_cast<uint4*>(kb_hi + off) = hi;
-            *reinterpret_cast<uint4*>(kb_lo + off) = lo;
-            tc::split8(xv, hi, lo);
-            *reinterpret_cast<uint4*>(vb_hi + off) = hi;
-            *reinterpret_cast<uint4*>(vb_lo + off) = lo;
-            tc::split8(xp, hi, lo);
-            *reinterpret_cast<uint4*>(rec + kKpHi + off) = hi;
-            *reinterpret_cast<uint4*>(rec + kKpLo + off) = lo;
-          }
+          for (int e = 0; e < 4; ++e) x[e] = bs * v[u][e];
+          put4_pair(qk_hi, qk_lo, t, 4 * lane, 2, x);
+        }
       }
       if (tid == 64) *reinterpret_cast<float*>(rec + kMeta) = expf(Gc);
     }
@@ -427,17 +418,21 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
     tc::fence_before();
     __syncthreads();
 
-    // 7. MMA 2, 3: W^T (cols 64..127) = (beta gamma k^)^T T^T;  U~^T (cols 128..191) = (beta v)^T T^T
+    // 7. MMA 2, 3: W^T (cols 64..127) = (beta gamma K^)^T T^T;  U~^T (cols 128..191) = (beta V)^T T^T,
+    //    A operands MN-major from the [s][d] rows (two 64-wide d atoms 1 KiB apart, 8-row s groups
+    //    2 KiB apart), B = T, K-major
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t id = tc::idesc_bf16(128, 64);
+      const uint32_t id = tc::idesc_bf16_amn(128, 64);
+      const uint32_t kh = tc::smem_addr(qk_hi) + 16384, kl = tc::smem_addr(qk_lo) + 16384;
+      const uint32_t vh = tc::smem_addr(qk_hi), vl = tc::smem_addr(qk_lo);
       for (int s = 0; s < 4; ++s) {
-        const uint32_t off = s * 32;
+        const uint32_t off = s * 32, aoff = s * 4096;
         const uint64_t th = tc::sdesc(tc::smem_addr(t_hi) + off, 1024), tl = tc::sdesc(tc::smem_addr(t_lo) + off, 1024);
-        tc::mma3(tmem + 64, tc::sdesc(tc::smem_addr(kb_hi) + off, 1024), tc::sdesc(tc::smem_addr(kb_lo) + off, 1024),
-                 th, tl, id, s == 0);
-        tc::mma3(tmem + 128, tc::sdesc(tc::smem_addr(vb_hi) + off, 1024), tc::sdesc(tc::smem_addr(vb_lo) + off, 1024),
-                 th, tl, id, s == 0);
+        tc::mma3(tmem + 64, tc::sdesc_lbo(kh + aoff, 1024, 2048), tc::sdesc_lbo(kl + aoff, 1024, 2048), th, tl, id,
+                 s == 0);
+        tc::mma3(tmem + 128, tc::sdesc_lbo(vh + aoff, 1024, 2048), tc::sdesc_lbo(vl + aoff, 1024, 2048), th, tl, id,
+                 s == 0);
       }
       tc::commit(&bar);
     }
@@ -684,12 +679,11 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     // S^T += K'^T U (three passes) -> commit (thread 0);  O += P U -> commit (thread 32)
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t id128 = tc::idesc_bf16_bmn(128, 32);
+      const uint32_t id128 = tc::idesc_bf16_abmn(128, 32);  // K' rows read MN-major
       const uint32_t bb = tc::smem_addr(buf), uh = tc::smem_addr(u_hi), ul = tc::smem_addr(u_lo);
       for (int s = 0; s < 4; ++s) {
-        const uint32_t off = s * 32;
-        tc::mma3(tS, tc::sdesc(bb + kKpHi + off, 1024), tc::sdesc(bb + kKpLo + off, 1024), tc::sdesc_mn32(uh + 1024 * s),
-                 tc::sdesc_mn32(ul + 1024 * s), id128, false);
+        tc::mma3(tS, tc::sdesc_lbo(bb + kKpHi + 4096 * s, 1024, 2048), tc::sdesc_lbo(bb + kKpLo + 4096 * s, 1024, 2048),
+                 tc::sdesc_mn32(uh + 1024 * s), tc::sdesc_mn32(ul + 1024 * s), id128, false);
       }
       tc::commit(&bar_mma[1]);
     } else if (tid == 32) {  // after its own first half, in issue order on this thread

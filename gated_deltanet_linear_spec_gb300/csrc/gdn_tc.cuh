@@ -43,6 +43,14 @@ __device__ __forceinline__ uint32_t mn32_off(int n, int k) {
   return (uint32_t)((k >> 3) * 512 + r * 64 + ((((n >> 3)) ^ ((r >> 1) & 3)) << 4) + (n & 7) * 2);
 }
 
+// Descriptor with an explicit leading-dimension offset, 128-byte swizzle.  Used for A operands
+// stored MN-major: a [k][m] tile laid out like a K-major one (64 m per 128-byte row, 8 k rows per
+// atom), lbo = the offset between the 64-wide m atoms, sbo = the offset between 8-row k groups.
+__device__ __forceinline__ uint64_t sdesc_lbo(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Descriptor of an N = 32 MN-major tile with the 64-byte swizzle (512-byte atoms along K).
 __device__ __forceinline__ uint64_t sdesc_mn32(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
@@ -54,8 +62,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// The same with the B operand MN-major.
+// The same with the B operand MN-major; with the A operand MN-major; with both.
 __host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
+__host__ __device__ constexpr uint32_t idesc_bf16_amn(int M, int N) { return idesc_bf16(M, N) | (1u << 15); }
+__host__ __device__ constexpr uint32_t idesc_bf16_abmn(int M, int N) { return idesc_bf16(M, N) | (3u << 15); }
 
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
