@@ -39,7 +39,7 @@ constexpr int kCh = kPrefillChunk;  // tokens per chunk
 constexpr int kD = 128;             // dk = dv on this path
 
 // Per (chunk, v-head) record written by the prep kernel, read by the scan kernel.
-constexpr uint32_t kWnHi = 0;       // -W   [t][dk]  bf16 hi image (K-major, 2 atoms)   16 KiB
+constexpr uint32_t kWnHi = 0;       // -W   [dk][t]  bf16 hi image (read MN-major)       16 KiB
 constexpr uint32_t kWnLo = 16384;   //               bf16 lo image                       16 KiB
 constexpr uint32_t kKpHi = 32768;   // K'   [s][dk]  bf16 hi image (2 atoms; read MN-major) 16 KiB
 constexpr uint32_t kKpLo = 49152;   //               bf16 lo image                       16 KiB
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
         for (int e = 0; e < 8; ++e) {
           const int s = 8 * j + e;
           const float qk = s < 32 ? v0[s & 31] : v1[s & 31];
-          x[e] = s <= t ? expf(Gt - sG[s]) * qk : 0.f;
+          x[e] = s <= t ? __expf(Gt - sG[s]) * qk : 0.f;
         }
         *reinterpret_cast<uint4*>(rec + kP + tc::img_off(t, 8 * j, 1)) = tc::pack8(x);
       }
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
         for (int e = 0; e < 4; ++e) {
           const int s = s0 + e;
           const float kk = s < 32 ? v0[s & 31] : v1[s & 31];
-          x[e] = s < t ? bt * expf(Gt - sG[s]) * kk : 0.f;
+          x[e] = s < t ? bt * __expf(Gt - sG[s]) * kk : 0.f;
         }
         *reinterpret_cast<float4*>(sA + t * kAStride + s0) = make_float4(x[0], x[1], x[2], x[3]);
       }
@@ -439,32 +439,28 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
     ok = __syncthreads_and(tc::mbar_wait(&bar, 1));
     if (ok) {
       tc::fence_after();
-      // 8. -W (hi/lo images, staged in shared memory) and U~ (fp32) from TMEM, lane = row d
+      // 8. -W and U~ (fp32) from TMEM, lane = row d: -W^T row d goes straight to the record as
+      //    row d of a [dk][t] image (read MN-major by the scan), eight 16-byte chunks per image
       const int d = 32 * warp + lane;
-      uint8_t* wn_hi = sm;  // the MMA 2/3 operands are consumed: reuse their space
-      uint8_t* wn_lo = sm + 16384;
       float* ut = reinterpret_cast<float*>(rec + kUt);
       for (int half = 0; half < 2; ++half) {
         float w[32];
         tc::tmem_ld32(tc::tmem_lane_col(tmem, warp, 64 + 32 * half), w);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x = -w[i];
-          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-          const uint32_t off = tc::img_off(32 * half + i, d, 2);
-          *reinterpret_cast<__nv_bfloat16*>(wn_hi + off) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(wn_lo + off) = lo;
+        for (int c = 0; c < 4; ++c) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = -w[8 * c + e];
+          uint4 hi, lo;
+          tc::split8(x, hi, lo);
+          const uint32_t off = tc::img_off(d, 32 * half + 8 * c, 1);
+          *reinterpret_cast<uint4*>(rec + kWnHi + off) = hi;
+          *reinterpret_cast<uint4*>(rec + kWnLo + off) = lo;
         }
         tc::tmem_ld32(tc::tmem_lane_col(tmem, warp, 128 + 32 * half), w);
 #pragma unroll
         for (int i = 0; i < 32; ++i) ut[((d >> 5) * kCh + 32 * half + i) * 32 + (d & 31)] = w[i];
       }
-      __syncthreads();
-      const uint4* src = reinterpret_cast<const uint4*>(sm);
-      uint4* dst = reinterpret_cast<uint4*>(rec + kWnHi);
-#pragma unroll 4
-      for (int i = tid; i < 32768 / 16; i += 128) dst[i] = src[i];
     }
   }
   if (!ok) {
@@ -610,22 +606,20 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     // U = -W S_0^T (three passes) -> commit (thread 0);  O = (gamma q^) S_0^T -> commit (thread 32)
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t id = tc::idesc_bf16_bmn(64, 32);
+      const uint32_t id = tc::idesc_bf16_abmn(64, 32);  // -W rows and S images both MN-major
       const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi), sl = tc::smem_addr(s_lo);
       for (int s = 0; s < 4; ++s) {  // first half of K into tU, the second half on thread 64
-        const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
-        tc::mma3(tU, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc_mn32(sh + 1024 * s),
-                 tc::sdesc_mn32(sl + 1024 * s), id, s == 0);
+        tc::mma3(tU, tc::sdesc_lbo(bb + kWnHi + 2048 * s, 16, 1024), tc::sdesc_lbo(bb + kWnLo + 2048 * s, 16, 1024),
+                 tc::sdesc_mn32(sh + 1024 * s), tc::sdesc_mn32(sl + 1024 * s), id, s == 0);
       }
       tc::commit(&bar_mma[0]);
     } else if (tid == 64) {
       tc::fence_after();
-      const uint32_t id = tc::idesc_bf16_bmn(64, 32);
+      const uint32_t id = tc::idesc_bf16_abmn(64, 32);
       const uint32_t bb = tc::smem_addr(buf), sh = tc::smem_addr(s_hi), sl = tc::smem_addr(s_lo);
       for (int s = 4; s < 8; ++s) {
-        const uint32_t off = (s >> 2) * 1024 + (s & 3) * 32;
-        tc::mma3(tU2, tc::sdesc(bb + kWnHi + off, 2048), tc::sdesc(bb + kWnLo + off, 2048), tc::sdesc_mn32(sh + 1024 * s),
-                 tc::sdesc_mn32(sl + 1024 * s), id, s == 4);
+        tc::mma3(tU2, tc::sdesc_lbo(bb + kWnHi + 2048 * s, 16, 1024), tc::sdesc_lbo(bb + kWnLo + 2048 * s, 16, 1024),
+                 tc::sdesc_mn32(sh + 1024 * s), tc::sdesc_mn32(sl + 1024 * s), id, s == 4);
       }
       tc::commit(&bar_mma[4]);
     } else if (tid == 32) {
