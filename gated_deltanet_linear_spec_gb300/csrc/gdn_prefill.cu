@@ -11,19 +11,18 @@
 //   U = U~ - W S_0^T,   O = diag(gamma) Q S_0^T + P U,  P[t,s] = e^{G_t - G_s} (q_t . k_s), s <= t
 //   S_c = gamma_c S_0 + U^T K',   K'_s = e^{G_c - G_s} k_s
 // Everything that does not depend on S_0 is computed for all chunks at once by the prep kernel
-// (one CTA per (row, chunk, v-head)); the scan kernel (one CTA per (row, v-head)) walks the
-// chunks in order, keeping the fp32 state in tensor memory.
+// (one CTA per (row, chunk, v-head)); the scan kernel (one CTA per (row, v-head, quarter of dv))
+// walks the chunks in order, keeping its 32 rows of the fp32 state in tensor memory.
 //
 // Tensor cores.  Every product is a tcgen05.mma (kind::f16, bf16 inputs, fp32 accumulation)
-// issued by one thread, with operands in 128B-swizzled shared memory and accumulators in TMEM.
-// Products that reach the state use a bf16 hi/lo split of both operands and three MMAs (about
-// 1e-5 relative error); the output-only products (S q and U P) use one.  All MMAs have M = 128:
-// they are arranged so the 128 rows are the head dimension or [q; k] stacked, e.g. W^T =
-// (beta gamma K)^T T^T.  The scan kernel's chunk inputs are written by the prep kernel as exact
-// shared-memory images and arrive with one bulk copy, prefetched while the previous chunk's
-// outputs are drained; its MMAs are committed in the order the state needs them (U, then the
-// state update, then the output), so the state readback never waits on output work.  T is
-// solved column by column on the CUDA cores.
+// with operands in swizzled shared memory and accumulators in TMEM.  Products that reach the
+// state use a bf16 hi/lo split of both operands and three MMAs (about 1e-5 relative error); the
+// output-only products use one.  Operands are K-major, or MN-major where that lets a thread
+// write its row of values as 16-byte chunks (a K-major [k][m] tile with the 128-byte swizzle is
+// read as the MN-major [m][k] operand; the scan's N = 32 operands use the 64-byte swizzle).
+// The prep kernel solves T = (I + A)^-1 on the CUDA cores in 16 x 16 blocks and writes every
+// chunk input of the scan as an exact shared-memory image; the scan copies a chunk's record in
+// with bulk copies two chunks ahead and spreads its MMA issue over three threads.
 //
 // Path limits: dk = dv = 128 and bf16 activations; other shapes use the token recurrence.
 // Every wait on an mbarrier is bounded; a timeout sets GDN_STATUS_WAIT_TIMEOUT, drains, frees
