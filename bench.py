@@ -58,11 +58,17 @@ def make_workload(name):
 
 
 def source_hash(*names) -> str:
+    """Hash of the kernel sources with comments and blank space removed, so that traffic recorded
+    for a kernel stays attached to it until its code changes."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "gated_deltanet_linear_spec_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "gated_deltanet_linear_spec_gb300", "csrc", n)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -3,7 +3,8 @@
 // Semantics ("[GDN] Spec-decoding-aware attention kernel", Changes, gated_delta_rule.hpp:
 // load slot spec_state_indices[n, num_accepted[n]-1], per-token store slot
 // spec_state_indices[n, t], slot <= 0 = no prior state / no store; the non-spec rows load and
-// store state_indices[n]).  Per (token, v-head h):
+// store state_indices[n], except that rows carrying their previous verify step's acceptance load
+// spec_state_indices[n, num_accepted-1]).  Per (token, v-head h):
 //   g = -exp(A_log[h]) softplus(a + dt_bias[h]),  beta = sigmoid(b),
 //   q^ = q / sqrt(|q|^2 + 1e-6) * scale,  k^ = k / sqrt(|k|^2 + 1e-6),
 //   S <- e^g S (I - beta k^ k^T) + beta v k^T,   o = S q^.
@@ -22,8 +23,9 @@
 // so both reductions run on the loaded state in one pass.  The prior state is issued as
 // streaming 128-bit loads before the token data is staged, so the state fetch overlaps the
 // norm/gate prologue -- and, in the mixed-batch path, the tail of the conv grid, which this
-// kernel follows as a programmatic dependent launch.  Each thread stores exactly the elements it loaded, after loading them,
-// so the load slot may also be a store slot (t = num_accepted-1) without a hazard.
+// kernel follows as a programmatic dependent launch.  Each thread stores exactly the elements
+// it loaded, after loading them, so the load slot may also be a store slot (t = num_accepted-1)
+// without a hazard.
 #include "gdn_internal.cuh"
 
 namespace gdn {
