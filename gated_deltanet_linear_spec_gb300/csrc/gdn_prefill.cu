@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
   __syncthreads();
 
   // 2. q^ (scaled) and k^ rows of the [q^; k^] images, and the gamma q^ record rows; warp w
-  //    takes tokens 16w .. 16w+15, four at a time so their loads are in flight together
+  //    takes tokens 16w .. 16w+15, eight at a time so their loads are in flight together
   for (int i0 = 0; i0 < 16; i0 += 8) {
     float q[8][4], k[8][4];
 #pragma unroll
