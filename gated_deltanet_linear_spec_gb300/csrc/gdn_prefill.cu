@@ -50,6 +50,7 @@ constexpr uint32_t kMeta = 122880;  // gamma_c (fp32)
 static_assert(kRecBytes >= kMeta + 16 && kUt == kImgBytes, "record layout");
 
 constexpr int kAStride = 68;  // floats per row of A in shared memory (16-byte aligned rows)
+constexpr int kPrepThreads = 256;  // 8 warps: warps w and w + 4 share TMEM lane quarter w
 constexpr int kPrepSmem = 81920 + kCh * kAStride * 4 + 1024;
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
@@ -93,9 +94,9 @@ __device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Prep: one CTA per (row, chunk, v-head); 128 threads.
+// Prep: one CTA per (row, chunk, v-head); 256 threads (8 warps).
 template <typename QT>
-__global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) {
+__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const PrefillLaunch p) {
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* sm = align1k(dyn_smem);
   uint8_t* qk_hi = sm;  // [q^; k^] [128][128] images (MMA 1); then [beta v; beta gamma k^] rows (MMA 2, 3)
@@ -159,12 +160,13 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
   __syncthreads();
 
   // 2. q^ (scaled) and k^ rows of the [q^; k^] images, and the gamma q^ record rows; warp w
-  //    takes tokens 16w .. 16w+15, eight at a time so their loads are in flight together
-  for (int i0 = 0; i0 < 16; i0 += 8) {
+  //    takes tokens 8w .. 8w+7, their loads in flight together
+  {
+    constexpr int i0 = 0;
     float q[8][4], k[8][4];
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
-      const int t = warp * 16 + i0 + b;
+      const int t = warp * 8 + i0 + b;
       if (t < nc) {
         const QT* row = qkv + (int64_t)(bos + t0 + t) * C;
         load4(row + qoff + 4 * lane, q[b]);
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
     }
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
-      const int t = warp * 16 + i0 + b;
+      const int t = warp * 8 + i0 + b;
       float sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -223,36 +225,35 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
   bool ok = __syncthreads_and(tc::mbar_wait(&bar, 0));
   if (ok) {
     tc::fence_after();
-    // 4. P rows to the record (warps 0, 1: q rows); A rows to shared memory (warps 2, 3: k rows)
-    float v0[32], v1[32];
-    tc::tmem_ld32(tc::tmem_lane_col(tmem, warp, 0), v0);
-    tc::tmem_ld32(tc::tmem_lane_col(tmem, warp, 32), v1);
-    const int t = (warp & 1) * 32 + lane;
+    // 4. P rows to the record (lane quarters 0, 1: q rows); A rows to shared memory (quarters
+    //    2, 3: k rows); warp w reads columns 32 (w / 4) .. +31 of its quarter's rows
+    const int quarter = warp & 3, chalf = warp >> 2;
+    float v0[32];
+    tc::tmem_ld32(tc::tmem_lane_col(tmem, quarter, 32 * chalf), v0);
+    const int t = (quarter & 1) * 32 + lane;
     const float Gt = sG[t];
-    if (warp < 2) {
+    if (quarter < 2) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int s = 8 * j + e;
-          const float qk = s < 32 ? v0[s & 31] : v1[s & 31];
-          x[e] = s <= t ? __expf(Gt - sG[s]) * qk : 0.f;
+          const int s = 32 * chalf + 8 * j + e;
+          x[e] = s <= t ? __expf(Gt - sG[s]) * v0[8 * j + e] : 0.f;
         }
-        *reinterpret_cast<uint4*>(rec + kP + tc::img_off(t, 8 * j, 1)) = tc::pack8(x);
+        *reinterpret_cast<uint4*>(rec + kP + tc::img_off(t, 32 * chalf + 8 * j, 1)) = tc::pack8(x);
       }
     } else {
       const float bt = sBeta[t];
 #pragma unroll
-      for (int s0 = 0; s0 < kCh; s0 += 4) {
+      for (int j = 0; j < 32; j += 4) {
         float x[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int s = s0 + e;
-          const float kk = s < 32 ? v0[s & 31] : v1[s & 31];
-          x[e] = s < t ? bt * __expf(Gt - sG[s]) * kk : 0.f;
+          const int s = 32 * chalf + j + e;
+          x[e] = s < t ? bt * __expf(Gt - sG[s]) * v0[j + e] : 0.f;
         }
-        *reinterpret_cast<float4*>(sA + t * kAStride + s0) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(sA + t * kAStride + 32 * chalf + j) = make_float4(x[0], x[1], x[2], x[3]);
       }
     }
     __syncthreads();
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
       //     beta_s gamma_s, and the rows beta_s v_s in the q^ half, which MMA 1 no longer needs;
       //     on the way, the record's K' rows e^{G_c - G_s} k^_s (the same image layout).
       const float Gc = sG[kCh - 1];
+      if (warp < 4) {
       for (int i = tid - 64; i < kCh * (kD / 8); i += 64) {
         const int t = i / (kD / 8), d0 = 8 * (i % (kD / 8));
         const uint32_t off = tc::img_off(kCh + t, d0, 2);
@@ -386,14 +388,13 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
         *reinterpret_cast<uint4*>(qk_hi + off) = nh;
         *reinterpret_cast<uint4*>(qk_lo + off) = nl;
       }
-      // v rows: warp 2 takes tokens 0..31, warp 3 tokens 32..63, sixteen at a time; lane = 4 dv
-      const int tw0 = (warp - 2) * 32;
-#pragma unroll 1
-      for (int i0 = 0; i0 < 32; i0 += 16) {
+      } else {
+        // v rows: warp 4 + i takes tokens 16i .. 16i+15, all loads in flight together; lane = 4 dv
+        const int tw0 = (warp - 4) * 16;
         float v[16][4];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const int t = tw0 + i0 + u;
+          const int t = tw0 + u;
           if (t < nc) {
             load4(qkv + (int64_t)(bos + t0 + t) * C + voff + 4 * lane, v[u]);
           } else {
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
         }
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const int t = tw0 + i0 + u;
+          const int t = tw0 + u;
           const float bs = sBeta[t];
           float x[4];
 #pragma unroll
@@ -438,28 +439,28 @@ __global__ void __launch_bounds__(128) chunk_prep_kernel(const PrefillLaunch p) 
     ok = __syncthreads_and(tc::mbar_wait(&bar, 1));
     if (ok) {
       tc::fence_after();
-      // 8. -W and U~ (fp32) from TMEM, lane = row d: -W^T row d goes straight to the record as
-      //    row d of a [dk][t] image (read MN-major by the scan), eight 16-byte chunks per image
-      const int d = 32 * warp + lane;
+      // 8. -W and U~ (fp32) from TMEM, lane = row d, warp w taking columns 32 (w / 4) .. +31:
+      //    -W^T row d goes straight to the record as row d of a [dk][t] image (read MN-major by
+      //    the scan), 16-byte chunks
+      const int quarter = warp & 3, half = warp >> 2;
+      const int d = 32 * quarter + lane;
       float* ut = reinterpret_cast<float*>(rec + kUt);
-      for (int half = 0; half < 2; ++half) {
-        float w[32];
-        tc::tmem_ld32(tc::tmem_lane_col(tmem, warp, 64 + 32 * half), w);
+      float w[32];
+      tc::tmem_ld32(tc::tmem_lane_col(tmem, quarter, 64 + 32 * half), w);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float x[8];
+      for (int c = 0; c < 4; ++c) {
+        float x[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = -w[8 * c + e];
-          uint4 hi, lo;
-          tc::split8(x, hi, lo);
-          const uint32_t off = tc::img_off(d, 32 * half + 8 * c, 1);
-          *reinterpret_cast<uint4*>(rec + kWnHi + off) = hi;
-          *reinterpret_cast<uint4*>(rec + kWnLo + off) = lo;
-        }
-        tc::tmem_ld32(tc::tmem_lane_col(tmem, warp, 128 + 32 * half), w);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ut[((d >> 5) * kCh + 32 * half + i) * 32 + (d & 31)] = w[i];
+        for (int e = 0; e < 8; ++e) x[e] = -w[8 * c + e];
+        uint4 hi, lo;
+        tc::split8(x, hi, lo);
+        const uint32_t off = tc::img_off(d, 32 * half + 8 * c, 1);
+        *reinterpret_cast<uint4*>(rec + kWnHi + off) = hi;
+        *reinterpret_cast<uint4*>(rec + kWnLo + off) = lo;
       }
+      tc::tmem_ld32(tc::tmem_lane_col(tmem, quarter, 128 + 32 * half), w);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ut[((d >> 5) * kCh + 32 * half + i) * 32 + (d & 31)] = w[i];
     }
   }
   if (!ok) {
@@ -753,7 +754,7 @@ cudaError_t launch_prep(const PrefillLaunch& p, int units, cudaStream_t s) {
     return cudaFuncSetAttribute(chunk_prep_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   });
   if (e != cudaSuccess) return e;
-  chunk_prep_kernel<QT><<<dim3(units, p.Hv), 128, kPrepSmem, s>>>(p);
+  chunk_prep_kernel<QT><<<dim3(units, p.Hv), kPrepThreads, kPrepSmem, s>>>(p);
   return cudaGetLastError();
 }
 
