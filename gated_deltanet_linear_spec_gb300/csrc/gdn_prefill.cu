@@ -93,6 +93,56 @@ __device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
   return -expf(A_log) * (x > 20.f ? x : log1pf(expf(x)));
 }
 
+// One 16 x 16 block T_ij of T = (I + A)^-1 (i > j), for the NR rows r0 .. r0+NR-1 of column c:
+// M = sum_{k=j}^{i-1} A_ik T_kj into sM (solve_m), then T_ij = -T_ii M (solve_t).  T is stored
+// transposed in the upper half of the A array (T[t][s] at sA[s][t]); in a diagonal block only
+// the entries on or above the diagonal of that storage are T.
+template <int NR>
+__device__ __forceinline__ void solve_m(const float* sA, float* sM, int i, int j, int c, int r0) {
+  float m[NR];
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) m[rr] = 0.f;
+#pragma unroll 1
+  for (int k = j; k < i; ++k) {
+#pragma unroll
+    for (int mm = 0; mm < 16; mm += 4) {
+      float4 tv = *reinterpret_cast<const float4*>(sA + (16 * j + c) * kAStride + 16 * k + mm);
+      if (k == j) {
+        tv.x = mm >= c ? tv.x : 0.f;
+        tv.y = mm + 1 >= c ? tv.y : 0.f;
+        tv.z = mm + 2 >= c ? tv.z : 0.f;
+        tv.w = mm + 3 >= c ? tv.w : 0.f;
+      }
+#pragma unroll
+      for (int rr = 0; rr < NR; ++rr) {
+        const float4 a = *reinterpret_cast<const float4*>(sA + (16 * i + r0 + rr) * kAStride + 16 * k + mm);
+        m[rr] = fmaf(a.x, tv.x, m[rr]);
+        m[rr] = fmaf(a.y, tv.y, m[rr]);
+        m[rr] = fmaf(a.z, tv.z, m[rr]);
+        m[rr] = fmaf(a.w, tv.w, m[rr]);
+      }
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) sM[(r0 + rr) * 16 + c] = m[rr];
+}
+
+template <int NR>
+__device__ __forceinline__ void solve_t(float* sA, const float* sM, int i, int j, int c, int r0) {
+  float acc[NR];
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) acc[rr] = 0.f;
+#pragma unroll
+  for (int mm = 0; mm < 16; ++mm) {  // T_ii[r][mm] (mm <= r) sits at row 16i+mm, column 16i+r
+    const float* trow = sA + (16 * i + mm) * kAStride + 16 * i + r0;
+    const float mv = sM[mm * 16 + c];
+#pragma unroll
+    for (int rr = 0; rr < NR; ++rr) acc[rr] = fmaf(mm <= r0 + rr ? trow[rr] : 0.f, mv, acc[rr]);
+  }
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) sA[(16 * j + c) * kAStride + 16 * i + r0 + rr] = -acc[rr];
+}
+
 // ------------------------------------------------------------------------------------------
 // Prep: one CTA per (row, chunk, v-head); 256 threads (8 warps).
 template <typename QT>
@@ -105,7 +155,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   uint8_t* t_hi = sm + 65536;  // T [64][64]
   uint8_t* t_lo = sm + 73728;
   __shared__ float sG[kCh], sBeta[kCh], sRk[kCh], sBG[kCh];
-  __shared__ float sMs[2][256];  // per-warp 16 x 16 scratch of the blocked solve
+  __shared__ float sMs[3][256];  // per-block 16 x 16 scratch of the blocked solve
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tmem_base;
 
@@ -258,12 +308,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     }
     __syncthreads();
 
-    if (warp < 2) {
-      // 5. T = (I + A)^-1 on warps 0-1 in 16 x 16 blocks: the diagonal blocks (I + A_bb)^-1 by
-      //    forward substitution, then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj in order of i - j.
-      //    T is kept transposed in the upper half of the A array: T[t][s] (t >= s) at sA[s][t]
-      //    (A is strictly lower, and A_ii is not read again once T_ii exists).
-      {
+    if (warp < 4) {
+      // 5. T = (I + A)^-1 on warps 0-3 in 16 x 16 blocks: the diagonal blocks (I + A_bb)^-1 by
+      //    forward substitution (warps 0-1), then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj in order
+      //    of i - j, the blocks of a distance spread over the four warps.  T is kept transposed
+      //    in the upper half of the A array: T[t][s] (t >= s) at sA[s][t] (A is strictly lower,
+      //    and A_ii is not read again once T_ii exists).
+      if (warp < 2) {
         const int o = 16 * (2 * warp + (lane >> 4)), c = lane & 15;
         float x[16];
 #pragma unroll
@@ -286,65 +337,34 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         for (int r = 0; r < 16; ++r)
           if (r >= c) sA[(o + c) * kAStride + o + r] = x[r];
       }
-      asm volatile("bar.sync 1, 64;" ::: "memory");
-      float* sM = sMs[warp];
-      const int c = lane & 15, r0 = (lane >> 4) * 8;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      const int c = lane & 15;
 #pragma unroll 1
       for (int dist = 1; dist < 4; ++dist) {
-#pragma unroll 1
-        for (int i = dist + warp; i < 4; i += 2) {
-          const int j = i - dist;
-          float m8[8];
-#pragma unroll
-          for (int rr = 0; rr < 8; ++rr) m8[rr] = 0.f;
-#pragma unroll 1
-          for (int k = j; k < i; ++k) {  // M = sum_k A_ik T_kj, rows r0.., column c
-#pragma unroll
-            for (int mm = 0; mm < 16; mm += 4) {
-              // T[16k+mm..][16j+c] sits transposed at row 16j+c; in the diagonal block only mm >= c
-              float4 tv = *reinterpret_cast<const float4*>(sA + (16 * j + c) * kAStride + 16 * k + mm);
-              if (k == j) {
-                tv.x = mm >= c ? tv.x : 0.f;
-                tv.y = mm + 1 >= c ? tv.y : 0.f;
-                tv.z = mm + 2 >= c ? tv.z : 0.f;
-                tv.w = mm + 3 >= c ? tv.w : 0.f;
-              }
-#pragma unroll
-              for (int rr = 0; rr < 8; ++rr) {
-                const float4 a = *reinterpret_cast<const float4*>(sA + (16 * i + r0 + rr) * kAStride + 16 * k + mm);
-                m8[rr] = fmaf(a.x, tv.x, m8[rr]);
-                m8[rr] = fmaf(a.y, tv.y, m8[rr]);
-                m8[rr] = fmaf(a.z, tv.z, m8[rr]);
-                m8[rr] = fmaf(a.w, tv.w, m8[rr]);
-              }
-            }
-          }
-#pragma unroll
-          for (int rr = 0; rr < 8; ++rr) sM[(r0 + rr) * 16 + c] = m8[rr];
-          __syncwarp();
-          float acc[8];
-#pragma unroll
-          for (int rr = 0; rr < 8; ++rr) acc[rr] = 0.f;
-#pragma unroll
-          for (int mm = 0; mm < 16; ++mm) {  // T_ij = -T_ii M;  T_ii[r][mm] (mm <= r) at row 16i+mm
-            const float4 t0 = *reinterpret_cast<const float4*>(sA + (16 * i + mm) * kAStride + 16 * i + r0);
-            const float4 t1 = *reinterpret_cast<const float4*>(sA + (16 * i + mm) * kAStride + 16 * i + r0 + 4);
-            const float tr[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-            const float mv = sM[mm * 16 + c];
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) acc[rr] = fmaf(mm <= r0 + rr ? tr[rr] : 0.f, mv, acc[rr]);
-          }
-#pragma unroll
-          for (int rr = 0; rr < 8; ++rr) sA[(16 * j + c) * kAStride + 16 * i + r0 + rr] = -acc[rr];
-          __syncwarp();
+        // distance 1: three blocks, one warp each; 2: two blocks, two warps each; 3: one block
+        const int wpb = dist == 1 ? 1 : (dist == 2 ? 2 : 4);
+        const int bi = warp / wpb, part = warp % wpb;
+        const bool active = dist + bi < 4;
+        const int i = dist + bi, j = i - dist;
+        float* sM = sMs[bi < 3 ? bi : 0];
+        if (active) {
+          if (dist == 1) solve_m<8>(sA, sM, i, j, c, (lane >> 4) * 8);
+          else if (dist == 2) solve_m<4>(sA, sM, i, j, c, part * 8 + (lane >> 4) * 4);
+          else solve_m<2>(sA, sM, i, j, c, part * 4 + (lane >> 4) * 2);
         }
-        asm volatile("bar.sync 1, 64;" ::: "memory");
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (active) {
+          if (dist == 1) solve_t<8>(sA, sM, i, j, c, (lane >> 4) * 8);
+          else if (dist == 2) solve_t<4>(sA, sM, i, j, c, part * 8 + (lane >> 4) * 4);
+          else solve_t<2>(sA, sM, i, j, c, part * 4 + (lane >> 4) * 2);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
       }
-      // 6a. T image (rows t, K = s): thread t of warps 0-1
+      // 6a. T image (rows t, K = s): row tid % 64, columns 32 (tid / 64) .. +31
       {
-        const int t2 = tid;
+        const int t2 = tid & 63, g0 = 32 * (tid >> 6);
 #pragma unroll
-        for (int g8 = 0; g8 < kCh; g8 += 8) {
+        for (int g8 = g0; g8 < g0 + 32; g8 += 8) {
           float x[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -359,13 +379,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         }
       }
     } else {
-      // 6b. meanwhile: the A operands of MMA 2 and 3, both read MN-major (a [s][d] tile laid out
-      //     like a K-major one): the k^ rows of the [q^; k^] images scaled in place by
-      //     beta_s gamma_s, and the rows beta_s v_s in the q^ half, which MMA 1 no longer needs;
-      //     on the way, the record's K' rows e^{G_c - G_s} k^_s (the same image layout).
+      // 6b. meanwhile, on warps 4-7: the A operands of MMA 2 and 3, both read MN-major (a [s][d]
+      //     tile laid out like a K-major one): the rows beta_s v_s in the q^ half, which MMA 1
+      //     no longer needs, and the k^ rows of the [q^; k^] images scaled in place by
+      //     beta_s gamma_s; on the way, the record's K' rows e^{G_c - G_s} k^_s (the same layout).
+      //     The v loads are issued first and stay in flight during the k^ pass.
       const float Gc = sG[kCh - 1];
-      if (warp < 4) {
-      for (int i = tid - 64; i < kCh * (kD / 8); i += 64) {
+      const int tw0 = (warp - 4) * 16;  // warp 4 + i takes v rows 16i .. 16i+15; lane = 4 dv
+      float v[16][4];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int t = tw0 + u;
+        if (t < nc) {
+          load4(qkv + (int64_t)(bos + t0 + t) * C + voff + 4 * lane, v[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[u][e] = 0.f;
+        }
+      }
+      for (int i = tid - 128; i < kCh * (kD / 8); i += 128) {
         const int t = i / (kD / 8), d0 = 8 * (i % (kD / 8));
         const uint32_t off = tc::img_off(kCh + t, d0, 2);
         const uint4 h = *reinterpret_cast<const uint4*>(qk_hi + off), l = *reinterpret_cast<const uint4*>(qk_lo + off);
@@ -388,31 +420,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         *reinterpret_cast<uint4*>(qk_hi + off) = nh;
         *reinterpret_cast<uint4*>(qk_lo + off) = nl;
       }
-      } else {
-        // v rows: warp 4 + i takes tokens 16i .. 16i+15, all loads in flight together; lane = 4 dv
-        const int tw0 = (warp - 4) * 16;
-        float v[16][4];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int t = tw0 + u;
-          if (t < nc) {
-            load4(qkv + (int64_t)(bos + t0 + t) * C + voff + 4 * lane, v[u]);
-          } else {
+      for (int u = 0; u < 16; ++u) {
+        const int t = tw0 + u;
+        const float bs = sBeta[t];
+        float x[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[u][e] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int t = tw0 + u;
-          const float bs = sBeta[t];
-          float x[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = bs * v[u][e];
-          put4_pair(qk_hi, qk_lo, t, 4 * lane, 2, x);
-        }
+        for (int e = 0; e < 4; ++e) x[e] = bs * v[u][e];
+        put4_pair(qk_hi, qk_lo, t, 4 * lane, 2, x);
       }
-      if (tid == 64) *reinterpret_cast<float*>(rec + kMeta) = expf(Gc);
+      if (tid == 128) *reinterpret_cast<float*>(rec + kMeta) = expf(Gc);
     }
     tc::fence_async_smem();
     tc::fence_before();
