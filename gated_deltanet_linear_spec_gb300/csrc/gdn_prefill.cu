@@ -653,6 +653,15 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     ++mma_commits[3];
     ++mma_commits[4];
     if (c > 0) store_outputs(c - 1);  // while the U products run
+    // this lane's U~ values (independent of the products): rows t of this warp sit in lanes
+    // 0..15 of its TMEM quarter; lanes 16..31 take over columns 16..31 of them
+    const int half = lane >> 4, t = 16 * warp + (lane & 15);
+    float4 utv[4];
+    {
+      const float4* ut = reinterpret_cast<const float4*>(buf + kBufUt) + t * 8 + 4 * half;
+#pragma unroll
+      for (int j4 = 0; j4 < 4; ++j4) utv[j4] = ut[j4];
+    }
     // Each warp goes on as soon as U is ready (the issuing thread's warp joins after issuing the
     // output products); the block-wide barrier comes only before the next products are issued.
     const bool u_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[0], mma_done[0] & 1) &&
@@ -663,22 +672,18 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     if (u_ok) {
       tc::fence_after();
       float u[32], u2[32];
-      tc::tmem_ld32(tc::tmem_lane_col(tU, warp, 0), u);
-      tc::tmem_ld32(tc::tmem_lane_col(tU2, warp, 0), u2);
+      tc::tmem_ld32x2(tc::tmem_lane_col(tU, warp, 0), u, tc::tmem_lane_col(tU2, warp, 0), u2);
 #pragma unroll
       for (int j = 0; j < 32; ++j) u[j] += u2[j];
-      // rows t of this warp sit in lanes 0..15; lanes 16..31 take over columns 16..31 of them
-      const int half = lane >> 4, t = 16 * warp + (lane & 15);
       float w16[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float hi_half = __shfl_sync(0xffffffffu, u[16 + j], lane & 15);
         w16[j] = half ? hi_half : u[j];
       }
-      const float4* ut = reinterpret_cast<const float4*>(buf + kBufUt) + t * 8 + 4 * half;
 #pragma unroll
       for (int j4 = 0; j4 < 4; ++j4) {
-        const float4 f = ut[j4];
+        const float4 f = utv[j4];
         w16[4 * j4] += f.x; w16[4 * j4 + 1] += f.y; w16[4 * j4 + 2] += f.z; w16[4 * j4 + 3] += f.w;
       }
       tc::put_mn32_row(u_hi, u_lo, t, w16, 2 * half, 2);
@@ -718,17 +723,19 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     bool tma_ok = true;
     if (s_ok) {
       tc::fence_after();
-      // the new state: images for the next chunk, then gamma_{c+1} S^T back into TMEM
+      // the new state: gamma_{c+1} S^T back into TMEM (in flight while the images for the next
+      // chunk are written)
       tc::tmem_ld32(tc::tmem_lane_col(tS, warp, 0), v);
       if (c + 1 < nch) {
-        tc::put_mn32_row(s_hi, s_lo, dk, v, 0, 4);
         const int nb = (c + 1) & 1;
         tma_ok = tc::mbar_wait(&bar_tma[nb], tma_done[nb] & 1);
         ++tma_done[nb];
         const float gn = *reinterpret_cast<const float*>(sm + nb * kBufBytes + kBufMeta);
+        float sv[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= gn;
-        tc::tmem_st32(tc::tmem_lane_col(tS, warp, 0), v);
+        for (int j = 0; j < 32; ++j) sv[j] = v[j] * gn;
+        tc::tmem_st32(tc::tmem_lane_col(tS, warp, 0), sv);
+        tc::put_mn32_row(s_hi, s_lo, dk, v, 0, 4);
       } else if (slot > 0) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) gS[(int64_t)j * kD] = v[j];
