@@ -371,7 +371,9 @@ def main() -> int:
         line = {"metric": METRIC, "value": ref["value"], "unit": UNIT, "n_gpus": 0, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": per_step_s * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": WORKLOADS[args.workload]}, "impl": "reference", "cpu_baseline": ref,
+                "config": {"workload": WORKLOADS[args.workload], "qkv_layout": args.qkv_layout,
+                           "conv_layout": args.conv_layout, "parallelism": "host CPU (oracle)"},
+                "impl": "reference", "cpu_baseline": ref,
                 "e2e": {"value": ref["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return 0
