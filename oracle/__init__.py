@@ -3,4 +3,4 @@
 Importable by the tests, the smoke check and the bench's CPU-baseline leg; never by the
 library.  See ``gdn_ref.c`` for what it computes and the passages it follows.
 """
-from .gdn_ref import Layer, Rows, build, conv_update, mixed_batch, recurrent  # noqa: F401
+from .gdn_ref import Layer, Rows, build, build_all, conv_update, mixed_batch, recurrent  # noqa: F401

@@ -5,7 +5,10 @@
  * bench's CPU-baseline leg may build, load or call this file.  It shares no code, header,
  * table or helper with the CUDA library, and it never reads a value the CUDA library wrote.
  *
- * What it computes is the plain definition, token by token, in double precision:
+ * What it computes is the plain definition, token by token, in double precision (the type
+ * `real` below).  A second build with -DGDN_REF_FLOAT takes the same steps in float; it exists
+ * only to measure the rounding noise that an fp32 implementation of the definition carries
+ * (the tests compare it with the double build, never with the CUDA library):
  *
  *   1. Split / gather.  Each subset of rows (speculative or not) sees its tokens through
  *      its own token_indx: x, a and b are all read at x[token_indx[i]], a[token_indx[i]],
@@ -57,6 +60,18 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+#ifdef GDN_REF_FLOAT
+typedef float real;
+#define R_EXP expf
+#define R_LOG1P log1pf
+#define R_SQRT sqrtf
+#else
+typedef double real;
+#define R_EXP exp
+#define R_LOG1P log1p
+#define R_SQRT sqrt
+#endif
 
 typedef struct {
   int32_t num_k_heads, num_v_heads, head_k_dim, head_v_dim;
@@ -120,9 +135,9 @@ static void act_copy(void* dst, int64_t di, const void* src, int64_t si, int bf1
 
 static int32_t global_token(const ref_rows* r, int32_t i) { return r->token_indx ? r->token_indx[i] : i; }
 
-static double softplus(double x) { return x > 20.0 ? x : log1p(exp(x)); }
-static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
-static double silu(double x) { return x / (1.0 + exp(-x)); }
+static real softplus(real x) { return x > (real)20 ? x : R_LOG1P(R_EXP(x)); }
+static real sigmoid(real x) { return (real)1 / ((real)1 + R_EXP(-x)); }
+static real silu(real x) { return x / ((real)1 + R_EXP(-x)); }
 
 /* ----------------------------------------------------------------------- row checks */
 
@@ -179,10 +194,10 @@ static int64_t x_channel(const ref_layer* L, int64_t c) {
 
 /*
  * Conv update of one subset.  conv_pool [P, state_len, C] (act type) is read and written;
- * y [num_tokens, C] (double, local token order) receives SiLU(conv).
+ * y [num_tokens, C] (real, local token order) receives SiLU(conv).
  */
 int gdn_ref_conv(const ref_layer* L, const void* conv_w, const void* conv_b, void* conv_pool,
-                 int64_t num_slots, const void* x, int32_t num_global, const ref_rows* rows, double* y) {
+                 int64_t num_slots, const void* x, int32_t num_global, const ref_rows* rows, real* y) {
   const int bf = L->act_is_bf16;
   const int32_t W = L->conv_width, SL = L->conv_state_len;
   const int64_t C = 2LL * L->num_k_heads * L->head_k_dim + (int64_t)L->num_v_heads * L->head_v_dim;
@@ -219,32 +234,32 @@ int gdn_ref_conv(const ref_layer* L, const void* conv_w, const void* conv_b, voi
     /* H = (W-1 history columns) ++ (the row's len inputs), kept both as exact values and as
      * the raw stored elements so that the slot write is a bit copy. */
     const int32_t hl = W - 1 + len;
-    double* H = (double*)malloc(sizeof(double) * (size_t)hl * (size_t)C);
+    real* H = (real*)malloc(sizeof(real) * (size_t)hl * (size_t)C);
     void* Hraw = malloc((size_t)hl * (size_t)C * (bf ? 2 : 4));
     if (!H || !Hraw) { free(H); free(Hraw); return -2; }
     for (int32_t i = 0; i < W - 1; ++i)
       for (int64_t c = 0; c < C; ++c) {
         if (read_prior) {
           int64_t src = ((int64_t)rd * SL + anchor + i) * C + c;
-          H[i * C + c] = act_get(conv_pool, src, bf);
+          H[i * C + c] = (real)act_get(conv_pool, src, bf);
           act_copy(Hraw, i * C + c, conv_pool, src, bf);
         } else {
-          H[i * C + c] = 0.0;
+          H[i * C + c] = (real)0;
           act_put(Hraw, i * C + c, bf, 0.0);
         }
       }
     for (int32_t t = 0; t < len; ++t) {
       int64_t gt = global_token(rows, bos + t);
       for (int64_t c = 0; c < C; ++c) {
-        H[(W - 1 + t) * C + c] = act_get(x, gt * C + x_channel(L, c), bf);
+        H[(W - 1 + t) * C + c] = (real)act_get(x, gt * C + x_channel(L, c), bf);
         act_copy(Hraw, (W - 1 + t) * C + c, x, gt * C + x_channel(L, c), bf);
       }
     }
     /* y_t[c] = SiLU(bias[c] + sum_i w[c][i] * H[t+i][c]) */
     for (int32_t t = 0; t < len; ++t)
       for (int64_t c = 0; c < C; ++c) {
-        double acc = conv_b ? act_get(conv_b, c, bf) : 0.0;
-        for (int32_t i = 0; i < W; ++i) acc += act_get(conv_w, c * W + i, bf) * H[(t + i) * C + c];
+        real acc = conv_b ? (real)act_get(conv_b, c, bf) : (real)0;
+        for (int32_t i = 0; i < W; ++i) acc += (real)act_get(conv_w, c * W + i, bf) * H[(t + i) * C + c];
         y[(int64_t)(bos + t) * C + c] = silu(acc);
       }
     /* Per-slot snapshots: after token t, its last W-1 inputs H[t+1 .. t+W-1] go to
@@ -278,12 +293,12 @@ typedef struct {
   const float* A_log;
   const float* dt_bias;
   float* ssm_pool;
-  const double* qkv;
+  const real* qkv;
   const void* a;
   const void* b;
   const ref_rows* rows;
   void* out;
-  double* out_f64;
+  real* out_f64;
 } rec_job;
 
 /* One (row, v-head) of one subset: load, token loop, stores. */
@@ -309,42 +324,42 @@ static void recurrent_row_head(const rec_job* J, int32_t n, int32_t h) {
     read_prior = load_slot > 0 && (r->has_initial_state ? r->has_initial_state[n] != 0 : 1);
   }
   const int64_t head_elems = (int64_t)dv * dk;
-  double* S = (double*)calloc((size_t)head_elems, sizeof(double));
-  double* qn = (double*)malloc(sizeof(double) * (size_t)dk);
-  double* kn = (double*)malloc(sizeof(double) * (size_t)dk);
+  real* S = (real*)calloc((size_t)head_elems, sizeof(real));
+  real* qn = (real*)malloc(sizeof(real) * (size_t)dk);
+  real* kn = (real*)malloc(sizeof(real) * (size_t)dk);
   if (!S || !qn || !kn) { free(S); free(qn); free(kn); return; }
   if (read_prior) {
     const float* src = J->ssm_pool + ((int64_t)load_slot * Hv + h) * head_elems;
-    for (int64_t e = 0; e < head_elems; ++e) S[e] = (double)src[e];
+    for (int64_t e = 0; e < head_elems; ++e) S[e] = (real)src[e];
   }
 
   for (int32_t t = 0; t < len; ++t) {
     const int64_t i = bos + t;
     const int64_t gt = global_token(r, (int32_t)i);
-    const double* q = J->qkv + i * C + (int64_t)kh * dk;
-    const double* k = J->qkv + i * C + (int64_t)Hk * dk + (int64_t)kh * dk;
-    const double* v = J->qkv + i * C + 2LL * Hk * dk + (int64_t)h * dv;
-    double sq = 0.0, sk = 0.0;
+    const real* q = J->qkv + i * C + (int64_t)kh * dk;
+    const real* k = J->qkv + i * C + (int64_t)Hk * dk + (int64_t)kh * dk;
+    const real* v = J->qkv + i * C + 2LL * Hk * dk + (int64_t)h * dv;
+    real sq = (real)0, sk = (real)0;
     for (int32_t c = 0; c < dk; ++c) { sq += q[c] * q[c]; sk += k[c] * k[c]; }
-    const double rq = 1.0 / sqrt(sq + L->norm_eps), rk = 1.0 / sqrt(sk + L->norm_eps);
-    for (int32_t c = 0; c < dk; ++c) { qn[c] = q[c] * rq * L->scale; kn[c] = k[c] * rk; }
+    const real rq = (real)1 / R_SQRT(sq + (real)L->norm_eps), rk = (real)1 / R_SQRT(sk + (real)L->norm_eps);
+    for (int32_t c = 0; c < dk; ++c) { qn[c] = q[c] * rq * (real)L->scale; kn[c] = k[c] * rk; }
 
-    const double av = act_get(J->a, gt * Hv + h, bf), bv = act_get(J->b, gt * Hv + h, bf);
-    const double g = -exp((double)J->A_log[h]) * softplus(av + (double)J->dt_bias[h]);
-    const double beta = sigmoid(bv);
-    const double decay = exp(g);
+    const real av = (real)act_get(J->a, gt * Hv + h, bf), bv = (real)act_get(J->b, gt * Hv + h, bf);
+    const real g = -R_EXP((real)J->A_log[h]) * softplus(av + (real)J->dt_bias[h]);
+    const real beta = sigmoid(bv);
+    const real decay = R_EXP(g);
 
     /* S <- e^g S ;  u = S k^ ;  S <- S + beta (v - u) k^T ;  o = S q^ */
     for (int64_t e = 0; e < head_elems; ++e) S[e] *= decay;
     for (int32_t row = 0; row < dv; ++row) {
-      double* s = S + (int64_t)row * dk;
-      double u = 0.0;
+      real* s = S + (int64_t)row * dk;
+      real u = (real)0;
       for (int32_t c = 0; c < dk; ++c) u += s[c] * kn[c];
-      const double delta = beta * (v[row] - u);
+      const real delta = beta * (v[row] - u);
       for (int32_t c = 0; c < dk; ++c) s[c] += delta * kn[c];
-      double o = 0.0;
+      real o = (real)0;
       for (int32_t c = 0; c < dk; ++c) o += s[c] * qn[c];
-      act_put(J->out, (gt * Hv + h) * dv + row, bf, o);
+      act_put(J->out, (gt * Hv + h) * dv + row, bf, (double)o);
       if (J->out_f64) J->out_f64[(gt * Hv + h) * dv + row] = o;
     }
     if (r->is_spec) {
@@ -384,14 +399,14 @@ static void* rec_worker_main(void* arg) {
 
 /*
  * Gated delta rule over one subset, for v-heads [h0, h1) (h1 <= 0 means all heads).
- * qkv [num_tokens, C] is the post-conv activation in local token order (double); a, b
+ * qkv [num_tokens, C] is the post-conv activation in local token order (real); a, b
  * [num_global, Hv] and out [num_global, Hv, dv] are in global token order (act type);
  * out_f64 (optional) receives the unrounded outputs.  Work is split over (row, head)
  * across nthreads POSIX threads; rows must use distinct slots.
  */
 int gdn_ref_recurrent(const ref_layer* L, const float* A_log, const float* dt_bias, float* ssm_pool,
-                      int64_t num_slots, const double* qkv, const void* a, const void* b, int32_t num_global,
-                      const ref_rows* rows, void* out, double* out_f64, int32_t h0, int32_t h1,
+                      int64_t num_slots, const real* qkv, const void* a, const void* b, int32_t num_global,
+                      const ref_rows* rows, void* out, real* out_f64, int32_t h0, int32_t h1,
                       int32_t nthreads) {
   if (L->num_v_heads % L->num_k_heads) return -1;
   for (int32_t n = 0; n < rows->num_seqs; ++n)

@@ -7,7 +7,9 @@ never receives a value that the CUDA library computed.
 
 Everything here is argument marshalling; the arithmetic is in ``gdn_ref.c``.  bf16 arrays
 travel as ``uint16`` bit patterns.  The functions mutate the pools they are given, exactly
-like the library does on the device.
+like the library does on the device.  ``precision="f64"`` (the oracle) works in double;
+``precision="f32"`` loads the float build of the same source, used only to measure the
+rounding noise of an fp32 implementation of the definition.
 """
 from __future__ import annotations
 
@@ -22,20 +24,29 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_ref.c")
-_LIB_PATH = os.path.join(_HERE, "libgdn_ref.so")
-_lib = None
+_LIB_PATHS = {"f64": os.path.join(_HERE, "libgdn_ref.so"), "f32": os.path.join(_HERE, "libgdn_ref_f32.so")}
+_REAL = {"f64": np.float64, "f32": np.float32}
+_libs: dict = {}
 _lock = threading.Lock()
 
 
-def build(force: bool = False) -> str:
-    """Compile ``gdn_ref.c`` into ``libgdn_ref.so`` beside it (portable C11, no -march)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+def build(force: bool = False, precision: str = "f64") -> str:
+    """Compile ``gdn_ref.c`` into ``libgdn_ref.so`` (or, for ``precision="f32"``, the float
+    build ``libgdn_ref_f32.so``) beside it (portable C11, no -march)."""
+    path = _LIB_PATHS[precision]
+    if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+        tmp = path + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
-               _SRC, "-o", tmp, "-lm"]
+               *(["-DGDN_REF_FLOAT"] if precision == "f32" else []), _SRC, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+        os.replace(tmp, path)
+    return path
+
+
+def build_all(force: bool = False) -> None:
+    """Both builds (the oracle and its float twin)."""
+    for precision in _LIB_PATHS:
+        build(force, precision)
 
 
 class _Layer(ctypes.Structure):
@@ -54,11 +65,10 @@ class _Rows(ctypes.Structure):
                 ("spec_cols", ctypes.c_int32), ("is_spec", ctypes.c_int32)]
 
 
-def _load():
-    global _lib
+def _load(precision: str = "f64"):
     with _lock:
-        if _lib is None:
-            lib = ctypes.CDLL(build())
+        if precision not in _libs:
+            lib = ctypes.CDLL(build(precision=precision))
             lib.gdn_ref_conv.restype = ctypes.c_int
             lib.gdn_ref_conv.argtypes = [ctypes.POINTER(_Layer), ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
@@ -69,8 +79,8 @@ def _load():
                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                               ctypes.POINTER(_Rows), ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
-            _lib = lib
-    return _lib
+            _libs[precision] = lib
+    return _libs[precision]
 
 
 @dataclass
@@ -142,16 +152,17 @@ def _need(a: np.ndarray, dtype, name: str) -> np.ndarray:
 
 
 def conv_update(layer: Layer, conv_w: np.ndarray, conv_b: Optional[np.ndarray], conv_pool: np.ndarray,
-                x: np.ndarray, num_global: int, rows: Rows) -> np.ndarray:
-    """Conv update of one subset; mutates ``conv_pool``; returns y [T_sub, C] (float64, local order)."""
+                x: np.ndarray, num_global: int, rows: Rows, precision: str = "f64") -> np.ndarray:
+    """Conv update of one subset; mutates ``conv_pool``; returns y [T_sub, C] (float64, or
+    float32 for the float build; local order)."""
     act = np.uint16 if layer.act_bf16 else np.float32
     _need(conv_w, act, "conv_w"); _need(conv_pool, act, "conv_pool"); _need(x, act, "x")
     if conv_b is not None:
         _need(conv_b, act, "conv_b")
-    y = np.zeros((rows.num_tokens, layer.channels), dtype=np.float64)
+    y = np.zeros((rows.num_tokens, layer.channels), dtype=_REAL[precision])
     keep: list = []
     L, R = layer._c(), rows._c(keep)
-    rc = _load().gdn_ref_conv(ctypes.byref(L), _ptr(conv_w), _ptr(conv_b), _ptr(conv_pool),
+    rc = _load(precision).gdn_ref_conv(ctypes.byref(L), _ptr(conv_w), _ptr(conv_b), _ptr(conv_pool),
                               int(conv_pool.shape[0]), _ptr(x), int(num_global), ctypes.byref(R), _ptr(y))
     if rc:
         raise ValueError(f"oracle conv rejected its inputs (rc={rc})")
@@ -161,18 +172,19 @@ def conv_update(layer: Layer, conv_w: np.ndarray, conv_b: Optional[np.ndarray], 
 def recurrent(layer: Layer, A_log: np.ndarray, dt_bias: np.ndarray, ssm_pool: np.ndarray,
               qkv: np.ndarray, a: np.ndarray, b: np.ndarray, num_global: int, rows: Rows,
               out: np.ndarray, out_f64: Optional[np.ndarray] = None, heads: Optional[tuple] = None,
-              nthreads: int = 1) -> None:
-    """Gated delta rule over one subset; mutates ``ssm_pool`` and ``out`` (and ``out_f64``)."""
+              nthreads: int = 1, precision: str = "f64") -> None:
+    """Gated delta rule over one subset; mutates ``ssm_pool`` and ``out`` (and ``out_f64``,
+    which like ``qkv`` is float64, or float32 for the float build)."""
     act = np.uint16 if layer.act_bf16 else np.float32
     _need(A_log, np.float32, "A_log"); _need(dt_bias, np.float32, "dt_bias")
-    _need(ssm_pool, np.float32, "ssm_pool"); _need(qkv, np.float64, "qkv")
+    _need(ssm_pool, np.float32, "ssm_pool"); _need(qkv, _REAL[precision], "qkv")
     _need(a, act, "a"); _need(b, act, "b"); _need(out, act, "out")
     if out_f64 is not None:
-        _need(out_f64, np.float64, "out_f64")
+        _need(out_f64, _REAL[precision], "out_f64")
     h0, h1 = heads if heads is not None else (0, 0)
     keep: list = []
     L, R = layer._c(), rows._c(keep)
-    rc = _load().gdn_ref_recurrent(ctypes.byref(L), _ptr(A_log), _ptr(dt_bias), _ptr(ssm_pool),
+    rc = _load(precision).gdn_ref_recurrent(ctypes.byref(L), _ptr(A_log), _ptr(dt_bias), _ptr(ssm_pool),
                                    int(ssm_pool.shape[0]), _ptr(qkv), _ptr(a), _ptr(b), int(num_global),
                                    ctypes.byref(R), _ptr(out), _ptr(out_f64), int(h0), int(h1),
                                    int(nthreads))
@@ -182,7 +194,7 @@ def recurrent(layer: Layer, A_log: np.ndarray, dt_bias: np.ndarray, ssm_pool: np
 
 def mixed_batch(layer: Layer, conv_w, conv_b, A_log, dt_bias, conv_pool, ssm_pool, x, a, b,
                 num_global: int, subsets: list, out: np.ndarray, out_f64: Optional[np.ndarray] = None,
-                heads: Optional[tuple] = None, nthreads: int = 1) -> None:
+                heads: Optional[tuple] = None, nthreads: int = 1, precision: str = "f64") -> None:
     """The whole path over a batch split into subsets (each a ``Rows``): conv, then recurrence.
 
     Each subset gathers x, a and b through its own token_indx and scatters its outputs back
@@ -191,5 +203,6 @@ def mixed_batch(layer: Layer, conv_w, conv_b, A_log, dt_bias, conv_pool, ssm_poo
     for rows in subsets:
         if rows.num_seqs == 0:
             continue
-        y = conv_update(layer, conv_w, conv_b, conv_pool, x, num_global, rows)
-        recurrent(layer, A_log, dt_bias, ssm_pool, y, a, b, num_global, rows, out, out_f64, heads, nthreads)
+        y = conv_update(layer, conv_w, conv_b, conv_pool, x, num_global, rows, precision)
+        recurrent(layer, A_log, dt_bias, ssm_pool, y, a, b, num_global, rows, out, out_f64, heads, nthreads,
+                  precision)

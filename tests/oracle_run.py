@@ -57,8 +57,9 @@ class OracleResult:
 
 def run_oracle(batch: Batch, heads: Optional[tuple] = None, nthreads: Optional[int] = None,
                subsets=("spec", "non_spec"), conv_pool: Optional[np.ndarray] = None,
-               ssm_pool: Optional[np.ndarray] = None) -> OracleResult:
-    """The whole path (conv, then gated delta rule) over the batch's subsets, on pool copies."""
+               ssm_pool: Optional[np.ndarray] = None, precision: str = "f64") -> OracleResult:
+    """The whole path (conv, then gated delta rule) over the batch's subsets, on pool copies.
+    ``precision="f32"`` runs the oracle's float build instead (a rounding-noise measurement)."""
     L = oracle_layer(batch)
     T, Hv, dv = batch.num_actual_tokens, batch.layer.num_v_heads, batch.layer.head_v_dim
     cp = np_act(batch.conv_pool) if conv_pool is None else conv_pool
@@ -68,14 +69,14 @@ def run_oracle(batch: Batch, heads: Optional[tuple] = None, nthreads: Optional[i
     cb = None if batch.conv_b is None else np_act(batch.conv_b)
     A_log, dt_bias = np_act(batch.A_log), np_act(batch.dt_bias)
     out = np.zeros((T, Hv, dv), dtype=x.dtype)
-    out_f64 = np.full((T, Hv, dv), np.nan)
+    out_f64 = np.full((T, Hv, dv), np.nan, dtype=np.float64 if precision == "f64" else np.float32)
     nthreads = nthreads or max(1, len(os.sched_getaffinity(0)))
     ys = {}
     for name in subsets:
         rows = oracle_rows(getattr(batch, name))
         if rows is None or rows.num_seqs == 0:
             continue
-        y = oracle.conv_update(L, w, cb, cp, x, T, rows)
+        y = oracle.conv_update(L, w, cb, cp, x, T, rows, precision)
         ys[name] = y
-        oracle.recurrent(L, A_log, dt_bias, sp, y, a, b, T, rows, out, out_f64, heads, nthreads)
+        oracle.recurrent(L, A_log, dt_bias, sp, y, a, b, T, rows, out, out_f64, heads, nthreads, precision)
     return OracleResult(cp, sp, out, out_f64, ys)
