@@ -14,7 +14,11 @@
 // GB300 design.  Decode/verify is fp32-state streaming: each (row, head) reads one 64 KiB state
 // and writes one per verify token, ~4 flops per byte, so the kernel is built for HBM, not the
 // tensor pipe.  Rows of S are independent (row i only needs s_i.k^, s_i.q^ and v_i), so one CTA
-// owns a (sequence, v-head, dv-tile of DVT rows) block and needs no cross-CTA exchange.  LPR
+// owns a (sequence, v-head, TPC dv-tiles of DVT rows) block and needs no cross-CTA exchange.
+// Most of a CTA's life is the latency of its dependent token-preparation loads (row metadata,
+// then q|k|v and the gates), so a CTA carries two tiles through one preparation: the second
+// tile's state arrives in shared memory by cp.async meanwhile and is swapped into registers
+// once the first tile's tokens are done.  LPR
 // lanes share a state row, each holding DK/LPR fp32 in registers; lane l of a row takes the
 // 16-byte words l, l+LPR, l+2*LPR, ... so every warp-wide 128-bit load/store covers
 // 32*16 bytes in LPR-word runs per row.  The two dot products per token are reduced with
@@ -71,8 +75,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 #define GDN_REC_MINB 8  // resident CTAs per SM the register allocation must allow
 #endif
 
-template <typename ACT, typename QT, int DK, int DVT, int LPR, int TB>
+template <typename ACT, typename QT, int DK, int DVT, int LPR, int TB, int TPC>
 __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const RecLaunch p) {
+  static_assert(TPC == 1 || TPC == 2, "one or two tiles per CTA");
   constexpr int NT = DVT * LPR;
   constexpr int EPT = DK / LPR;  // fp32 state elements per thread
   constexpr int NV = EPT / 4;    // float4 words per thread
@@ -83,8 +88,11 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
 
   __shared__ __align__(16) float sQ[TB][DK];
   __shared__ __align__(16) float sK[TB][DK];
-  __shared__ __align__(16) float sV[TB][DVT];
-  __shared__ float sO[TB][DVT];
+  __shared__ __align__(16) float sV[TB][DVT * TPC];
+  __shared__ float sO[TB][DVT * TPC];
+  // the second tile's state while the first one is in registers (each thread only touches the
+  // elements it owns, so no barrier guards it)
+  __shared__ __align__(16) float4 sSt[TPC > 1 ? NT * NV : 1];
   __shared__ float sEg[TB], sBeta[TB], sKQ[TB];
   __shared__ int32_t sStore[TB], sGt[TB];
 
@@ -93,7 +101,7 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   const int ln = tid % LPR;  // lane within the row
   const int h = blockIdx.y;
   const int kh = h / (p.Hv / p.Hk);
-  const int dv0 = blockIdx.x * DVT;
+  const int dv0 = blockIdx.x * DVT * TPC;
   const int z = blockIdx.z;
   const int s = z < p.rows0 ? 0 : 1;
   const RowsDev R = p.sub[s];
@@ -127,16 +135,31 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   const int64_t row_off = ((int64_t)h * p.dv + dv0 + rr) * DK;  // within one slot
   const int64_t slot_elems = (int64_t)p.Hv * head_elems;
 
-  // 1. prior state -> registers (streaming loads, issued first)
+  // 1. prior state -> registers (streaming loads, issued first); a second tile's state goes to
+  //    shared memory through cp.async, in flight during the token preparation
   float4 S[NV];
   if (read_prior) {
     const float4* src = reinterpret_cast<const float4*>(p.ssm_pool + load_slot * slot_elems + row_off) + ln;
 #pragma unroll
     for (int i = 0; i < NV; ++i) S[i] = ld_stream_f4(src + i * LPR);
+    if constexpr (TPC > 1) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(
+                         &sSt[i * NT + tid])),
+                     "l"(src + (int64_t)DVT * DK / 4 + i * LPR)
+                     : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < NV; ++i) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (TPC > 1) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) sSt[i * NT + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
+  int reg_tile = 0;  // which of the CTA's tiles the registers hold
 
   // row checks (the loads above stay in flight)
   int L = eos - bos;
@@ -148,6 +171,7 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   else if (bad_accept) skip = GDN_STATUS_NUM_ACCEPTED;
   if (skip) {
     if (reporter && skip != 0x80000000u) set_status(p.status, skip);
+    if constexpr (TPC > 1) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
     return;
   }
   if (!slot_ok && reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
@@ -172,8 +196,8 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
     //     round trip: raw q and k rows and this tile's v slice land in shared memory through
     //     cp.async (no registers held), the gate inputs and store slots through lane 0 of each
     //     token's warp.  Warp w prepares tokens w, w+NWARP, ...
-    if constexpr (sizeof(QT) == 4 && DK % 4 == 0 && DVT % 4 == 0) {
-      constexpr int QC = DK / 4, VC = DVT / 4;  // 16-byte chunks per q/k row and per v slice
+    if constexpr (sizeof(QT) == 4 && DK % 4 == 0 && (DVT * TPC) % 4 == 0) {
+      constexpr int QC = DK / 4, VC = DVT * TPC / 4;  // 16-byte chunks per q/k row and per v slice
       for (int idx = tid; idx < nt * (2 * QC + VC); idx += NT) {
         const int t = idx / (2 * QC + VC), c = idx % (2 * QC + VC);
         const int64_t i = bos + tb0 + t;
@@ -194,8 +218,8 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
                      : "memory");
       }
     } else {
-      for (int idx = tid; idx < nt * (2 * DK + DVT); idx += NT) {
-        const int t = idx / (2 * DK + DVT), c = idx % (2 * DK + DVT);
+      for (int idx = tid; idx < nt * (2 * DK + DVT * TPC); idx += NT) {
+        const int t = idx / (2 * DK + DVT * TPC), c = idx % (2 * DK + DVT * TPC);
         const int64_t i = bos + tb0 + t;
         if (c < DK) sQ[t][c] = to_f32(qkv[i * p.C + (int64_t)kh * DK + c]);
         else if (c < 2 * DK) sK[t][c - DK] = to_f32(qkv[i * p.C + (int64_t)p.Hk * DK + (int64_t)kh * DK + c - DK]);
@@ -268,45 +292,60 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
     }
     __syncthreads();
 
-    // 3. the recurrence, token by token
-    for (int t = 0; t < nt; ++t) {
-      const float4* k4 = reinterpret_cast<const float4*>(sK[t]) + ln;
-      const float4* q4 = reinterpret_cast<const float4*>(sQ[t]) + ln;
-      float dk_ = 0.f, dq_ = 0.f;
+    // 3. the recurrence, token by token, for the tile in registers and then (with two tiles)
+    //    for the other one, swapped in from shared memory
+#pragma unroll 1
+    for (int pass = 0; pass < TPC; ++pass) {
+      if (pass == 1) {
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const float4 kf = k4[i * LPR], qf = q4[i * LPR];
-        dk_ = fmaf(S[i].x, kf.x, fmaf(S[i].y, kf.y, fmaf(S[i].z, kf.z, fmaf(S[i].w, kf.w, dk_))));
-        dq_ = fmaf(S[i].x, qf.x, fmaf(S[i].y, qf.y, fmaf(S[i].z, qf.z, fmaf(S[i].w, qf.w, dq_))));
+        for (int i = 0; i < NV; ++i) {
+          const float4 o = sSt[i * NT + tid];
+          sSt[i * NT + tid] = S[i];
+          S[i] = o;
+        }
+        reg_tile ^= 1;
       }
+      const int col = reg_tile * DVT + rr;  // this thread's state row among the CTA's rows
+      const int64_t tile_off = row_off + (int64_t)reg_tile * DVT * DK;
+      for (int t = 0; t < nt; ++t) {
+        const float4* k4 = reinterpret_cast<const float4*>(sK[t]) + ln;
+        const float4* q4 = reinterpret_cast<const float4*>(sQ[t]) + ln;
+        float dk_ = 0.f, dq_ = 0.f;
 #pragma unroll
-      for (int o = LPR / 2; o >= 1; o >>= 1) {
-        dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
-        dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
-      }
-      const float eg = sEg[t], beta = sBeta[t];
-      const float delta = beta * (sV[t][rr] - eg * dk_);
+        for (int i = 0; i < NV; ++i) {
+          const float4 kf = k4[i * LPR], qf = q4[i * LPR];
+          dk_ = fmaf(S[i].x, kf.x, fmaf(S[i].y, kf.y, fmaf(S[i].z, kf.z, fmaf(S[i].w, kf.w, dk_))));
+          dq_ = fmaf(S[i].x, qf.x, fmaf(S[i].y, qf.y, fmaf(S[i].z, qf.z, fmaf(S[i].w, qf.w, dq_))));
+        }
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const float4 kf = k4[i * LPR];
-        S[i].x = fmaf(delta, kf.x, eg * S[i].x);
-        S[i].y = fmaf(delta, kf.y, eg * S[i].y);
-        S[i].z = fmaf(delta, kf.z, eg * S[i].z);
-        S[i].w = fmaf(delta, kf.w, eg * S[i].w);
-      }
-      if (ln == 0) sO[t][rr] = fmaf(delta, sKQ[t], eg * dq_);
-      const int ss = sStore[t];
-      if (ss > 0) {
-        float4* dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off) + ln;
+        for (int o = LPR / 2; o >= 1; o >>= 1) {
+          dk_ += __shfl_xor_sync(0xffffffffu, dk_, o);
+          dq_ += __shfl_xor_sync(0xffffffffu, dq_, o);
+        }
+        const float eg = sEg[t], beta = sBeta[t];
+        const float delta = beta * (sV[t][col] - eg * dk_);
 #pragma unroll
-        for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, S[i]);
+        for (int i = 0; i < NV; ++i) {
+          const float4 kf = k4[i * LPR];
+          S[i].x = fmaf(delta, kf.x, eg * S[i].x);
+          S[i].y = fmaf(delta, kf.y, eg * S[i].y);
+          S[i].z = fmaf(delta, kf.z, eg * S[i].z);
+          S[i].w = fmaf(delta, kf.w, eg * S[i].w);
+        }
+        if (ln == 0) sO[t][col] = fmaf(delta, sKQ[t], eg * dq_);
+        const int ss = sStore[t];
+        if (ss > 0) {
+          float4* dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + tile_off) + ln;
+#pragma unroll
+          for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, S[i]);
+        }
       }
     }
     __syncthreads();
 
     // 4. outputs, scattered to the tokens' global positions
-    for (int idx = tid; idx < nt * DVT; idx += NT) {
-      const int t = idx / DVT, r = idx % DVT;
+    for (int idx = tid; idx < nt * DVT * TPC; idx += NT) {
+      const int t = idx / (DVT * TPC), r = idx % (DVT * TPC);
       const int gt = sGt[t];
       if (gt >= 0) out[((int64_t)gt * p.Hv + h) * p.dv + dv0 + r] = from_f32<ACT>(sO[t][r]);
     }
@@ -317,13 +356,21 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
     if (ss >= p.num_slots) {
       if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
     } else if (ss > 0) {
-      float4* dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off) + ln;
+      float4* dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off + (int64_t)reg_tile * DVT * DK) + ln;
 #pragma unroll
       for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, S[i]);
+      if constexpr (TPC > 1) {  // the other tile, from shared memory
+        dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off + (int64_t)(reg_tile ^ 1) * DVT * DK) + ln;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, sSt[i * NT + tid]);
+      }
     }
   }
 }
 
+#ifndef GDN_REC_TPC
+#define GDN_REC_TPC 2  // tiles of state rows per CTA (2: two tiles share one token preparation)
+#endif
 #ifndef GDN_REC_DVT
 #define GDN_REC_DVT 16  // state rows per CTA
 #endif
@@ -331,11 +378,11 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
 #define GDN_REC_LPR 8  // lanes per state row (16 fp32 each at dk = 128)
 #endif
 
-template <typename ACT, typename QT, int DK, int DVT>
+template <typename ACT, typename QT, int DK, int DVT, int TPC>
 static cudaError_t launch_tile(const RecLaunch& p, int rows, bool pdl, cudaStream_t s) {
   constexpr int LPR = (DK / GDN_REC_LPR >= 4) ? GDN_REC_LPR : DK / 4;
   constexpr int TB = 8;
-  const int tiles = p.dv / DVT;
+  const int tiles = p.dv / (DVT * TPC);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles, p.Hv, rows);
   cfg.blockDim = dim3(DVT * LPR);
@@ -350,17 +397,25 @@ static cudaError_t launch_tile(const RecLaunch& p, int rows, bool pdl, cudaStrea
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, recurrent_kernel<ACT, QT, DK, DVT, LPR, TB>, p);
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel<ACT, QT, DK, DVT, LPR, TB, TPC>, p);
+}
+
+// Two tiles per CTA when dv holds an even number of them (one token preparation serves both),
+// else one.
+template <typename ACT, typename QT, int DK>
+static cudaError_t launch_dv(const RecLaunch& p, int rows, bool pdl, cudaStream_t s) {
+  if (GDN_REC_TPC == 2 && p.dv % (2 * GDN_REC_DVT) == 0) return launch_tile<ACT, QT, DK, GDN_REC_DVT, 2>(p, rows, pdl, s);
+  if (p.dv % GDN_REC_DVT == 0) return launch_tile<ACT, QT, DK, GDN_REC_DVT, 1>(p, rows, pdl, s);
+  return launch_tile<ACT, QT, DK, 16, 1>(p, rows, pdl, s);
 }
 
 template <typename ACT, typename QT>
 static cudaError_t launch_dk(const RecLaunch& p, int rows, bool pdl, cudaStream_t s) {
-  const bool big = (p.dv % GDN_REC_DVT) == 0;
   switch (p.dk) {
-    case 16: return big ? launch_tile<ACT, QT, 16, GDN_REC_DVT>(p, rows, pdl, s) : launch_tile<ACT, QT, 16, 16>(p, rows, pdl, s);
-    case 32: return big ? launch_tile<ACT, QT, 32, GDN_REC_DVT>(p, rows, pdl, s) : launch_tile<ACT, QT, 32, 16>(p, rows, pdl, s);
-    case 64: return big ? launch_tile<ACT, QT, 64, GDN_REC_DVT>(p, rows, pdl, s) : launch_tile<ACT, QT, 64, 16>(p, rows, pdl, s);
-    case 128: return big ? launch_tile<ACT, QT, 128, GDN_REC_DVT>(p, rows, pdl, s) : launch_tile<ACT, QT, 128, 16>(p, rows, pdl, s);
+    case 16: return launch_dv<ACT, QT, 16>(p, rows, pdl, s);
+    case 32: return launch_dv<ACT, QT, 32>(p, rows, pdl, s);
+    case 64: return launch_dv<ACT, QT, 64>(p, rows, pdl, s);
+    case 128: return launch_dv<ACT, QT, 128>(p, rows, pdl, s);
     default: return cudaErrorInvalidValue;
   }
 }
