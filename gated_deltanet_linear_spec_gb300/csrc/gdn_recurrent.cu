@@ -77,7 +77,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <typename ACT, typename QT, int DK, int DVT, int LPR, int TB, int TPC>
 __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const RecLaunch p) {
-  static_assert(TPC == 1 || TPC == 2, "one or two tiles per CTA");
+  static_assert(TPC == 1 || TPC == 2 || TPC == 4, "1, 2 or 4 tiles per CTA");
   constexpr int NT = DVT * LPR;
   constexpr int EPT = DK / LPR;  // fp32 state elements per thread
   constexpr int NV = EPT / 4;    // float4 words per thread
@@ -90,9 +90,9 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   __shared__ __align__(16) float sK[TB][DK];
   __shared__ __align__(16) float sV[TB][DVT * TPC];
   __shared__ float sO[TB][DVT * TPC];
-  // the second tile's state while the first one is in registers (each thread only touches the
-  // elements it owns, so no barrier guards it)
-  __shared__ __align__(16) float4 sSt[TPC > 1 ? NT * NV : 1];
+  // the states of the tiles not in registers, one slot each (each thread only touches the
+  // elements it owns, so no barrier guards them)
+  __shared__ __align__(16) float4 sSt[TPC > 1 ? (TPC - 1) * NV * NT : 1];
   __shared__ float sEg[TB], sBeta[TB], sKQ[TB];
   __shared__ int32_t sStore[TB], sGt[TB];
 
@@ -144,11 +144,13 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
     for (int i = 0; i < NV; ++i) S[i] = ld_stream_f4(src + i * LPR);
     if constexpr (TPC > 1) {
 #pragma unroll
-      for (int i = 0; i < NV; ++i)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(
-                         &sSt[i * NT + tid])),
-                     "l"(src + (int64_t)DVT * DK / 4 + i * LPR)
-                     : "memory");
+      for (int k = 0; k < TPC - 1; ++k)
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(
+                           &sSt[(k * NV + i) * NT + tid])),
+                       "l"(src + (int64_t)(k + 1) * DVT * DK / 4 + i * LPR)
+                       : "memory");
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
   } else {
@@ -156,10 +158,13 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
     for (int i = 0; i < NV; ++i) S[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if constexpr (TPC > 1) {
 #pragma unroll
-      for (int i = 0; i < NV; ++i) sSt[i * NT + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < (TPC - 1) * NV; ++i) sSt[i * NT + tid] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  int reg_tile = 0;  // which of the CTA's tiles the registers hold
+  // tile_at[0]: the tile whose state is in registers; tile_at[k]: the tile in slot k - 1
+  int tile_at[TPC];
+#pragma unroll
+  for (int k = 0; k < TPC; ++k) tile_at[k] = k;
 
   // row checks (the loads above stay in flight)
   int L = eos - bos;
@@ -292,21 +297,23 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
     }
     __syncthreads();
 
-    // 3. the recurrence, token by token, for the tile in registers and then (with two tiles)
-    //    for the other one, swapped in from shared memory
-#pragma unroll 1
+    // 3. the recurrence, token by token, for the tile in registers and then for each other
+    //    tile, swapped in from its shared-memory slot
+#pragma unroll
     for (int pass = 0; pass < TPC; ++pass) {
-      if (pass == 1) {
+      if (pass > 0) {
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
-          const float4 o = sSt[i * NT + tid];
-          sSt[i * NT + tid] = S[i];
+          const float4 o = sSt[((pass - 1) * NV + i) * NT + tid];
+          sSt[((pass - 1) * NV + i) * NT + tid] = S[i];
           S[i] = o;
         }
-        reg_tile ^= 1;
+        const int t_ = tile_at[0];
+        tile_at[0] = tile_at[pass];
+        tile_at[pass] = t_;
       }
-      const int col = reg_tile * DVT + rr;  // this thread's state row among the CTA's rows
-      const int64_t tile_off = row_off + (int64_t)reg_tile * DVT * DK;
+      const int col = tile_at[0] * DVT + rr;  // this thread's state row among the CTA's rows
+      const int64_t tile_off = row_off + (int64_t)tile_at[0] * DVT * DK;
       for (int t = 0; t < nt; ++t) {
         const float4* k4 = reinterpret_cast<const float4*>(sK[t]) + ln;
         const float4* q4 = reinterpret_cast<const float4*>(sQ[t]) + ln;
@@ -356,20 +363,21 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
     if (ss >= p.num_slots) {
       if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
     } else if (ss > 0) {
-      float4* dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off + (int64_t)reg_tile * DVT * DK) + ln;
+      float4* dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off + (int64_t)tile_at[0] * DVT * DK) + ln;
 #pragma unroll
       for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, S[i]);
-      if constexpr (TPC > 1) {  // the other tile, from shared memory
-        dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off + (int64_t)(reg_tile ^ 1) * DVT * DK) + ln;
 #pragma unroll
-        for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, sSt[i * NT + tid]);
+      for (int k = 1; k < TPC; ++k) {  // the other tiles, from their slots
+        dst = reinterpret_cast<float4*>(p.ssm_pool + ss * slot_elems + row_off + (int64_t)tile_at[k] * DVT * DK) + ln;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) st_f4(dst + i * LPR, sSt[((k - 1) * NV + i) * NT + tid]);
       }
     }
   }
 }
 
 #ifndef GDN_REC_TPC
-#define GDN_REC_TPC 2  // tiles of state rows per CTA (2: two tiles share one token preparation)
+#define GDN_REC_TPC 2  // most tiles of state rows per CTA (they share one token preparation)
 #endif
 #ifndef GDN_REC_DVT
 #define GDN_REC_DVT 16  // state rows per CTA
@@ -400,11 +408,12 @@ static cudaError_t launch_tile(const RecLaunch& p, int rows, bool pdl, cudaStrea
   return cudaLaunchKernelEx(&cfg, recurrent_kernel<ACT, QT, DK, DVT, LPR, TB, TPC>, p);
 }
 
-// Two tiles per CTA when dv holds an even number of them (one token preparation serves both),
-// else one.
+// As many tiles per CTA (up to GDN_REC_TPC) as dv holds evenly: one token preparation serves
+// them all.
 template <typename ACT, typename QT, int DK>
 static cudaError_t launch_dv(const RecLaunch& p, int rows, bool pdl, cudaStream_t s) {
-  if (GDN_REC_TPC == 2 && p.dv % (2 * GDN_REC_DVT) == 0) return launch_tile<ACT, QT, DK, GDN_REC_DVT, 2>(p, rows, pdl, s);
+  if (GDN_REC_TPC >= 4 && p.dv % (4 * GDN_REC_DVT) == 0) return launch_tile<ACT, QT, DK, GDN_REC_DVT, 4>(p, rows, pdl, s);
+  if (GDN_REC_TPC >= 2 && p.dv % (2 * GDN_REC_DVT) == 0) return launch_tile<ACT, QT, DK, GDN_REC_DVT, 2>(p, rows, pdl, s);
   if (p.dv % GDN_REC_DVT == 0) return launch_tile<ACT, QT, DK, GDN_REC_DVT, 1>(p, rows, pdl, s);
   return launch_tile<ACT, QT, DK, 16, 1>(p, rows, pdl, s);
 }
