@@ -16,12 +16,12 @@
 // tensor pipe.  Rows of S are independent (row i only needs s_i.k^, s_i.q^ and v_i), so one CTA
 // owns a (sequence, v-head, TPC dv-tiles of DVT rows) block and needs no cross-CTA exchange.
 // Most of a CTA's life is the latency of its dependent token-preparation loads (row metadata,
-// then q|k|v and the gates), so a CTA carries two tiles through one preparation: the second
-// tile's state arrives in shared memory by cp.async meanwhile and is swapped into registers
-// once the first tile's tokens are done.  LPR
-// lanes share a state row, each holding DK/LPR fp32 in registers; lane l of a row takes the
-// 16-byte words l, l+LPR, l+2*LPR, ... so every warp-wide 128-bit load/store covers
-// 32*16 bytes in LPR-word runs per row.  The two dot products per token are reduced with
+// then q|k|v and the gates), so a CTA carries TPC tiles (two by default) through one
+// preparation: the other tiles' states arrive in shared memory by cp.async meanwhile and are
+// swapped into registers in turn once the previous tile's tokens are done.  LPR lanes share a
+// state row, each holding DK/LPR fp32 in registers; lane l of a row takes the 16-byte words
+// l, l+LPR, l+2*LPR, ... so every warp-wide 128-bit load/store covers 32*16 bytes in LPR-word
+// runs per row.  The two dot products per token are reduced with
 // xor-shuffles inside the row's lanes, using
 //   S_t q^ = e^g (S_{t-1} q^) + delta (k^.q^),  delta = beta (v - e^g S_{t-1} k^),
 // so both reductions run on the loaded state in one pass.  The prior state is issued as
