@@ -83,7 +83,7 @@ int ntok(const gdn_rows* r) { return r ? r->num_tokens : 0; }
 int conv_units(const gdn_rows* r) {
   if (!r || r->num_seqs == 0) return 0;
   if (is_spec(r)) return r->num_seqs;
-  return (r->num_tokens + kConvSeg - 1) / kConvSeg + r->num_seqs;
+  return (r->num_tokens + kConvSegNS - 1) / kConvSegNS + r->num_seqs;
 }
 
 // Chunk units of the prefill rows: an upper bound from the subset's token count.

@@ -15,7 +15,7 @@
 // it loads the slot's history into registers before anything else, and from then on it is the
 // only reader and writer of those slot elements, so it writes the rolled columns as the tokens
 // stream through -- no tmp buffer, no second launch, no race.  Long non-spec rows are cut into
-// 64-token segments for parallelism; segment 0 alone touches the slot (it fetches the row's last
+// 16-token segments for parallelism; segment 0 alone touches the slot (it fetches the row's last
 // W-1 inputs for the write-back when the row is longer than one segment), later segments rebuild
 // their window from x.  All accesses are 16-byte vectors along the channel axis (8 bf16 or
 // 2x4 fp32 per thread); the token index and x loads of 4 tokens are issued together.
@@ -44,7 +44,7 @@ __device__ __forceinline__ int64_t x_channel(const ConvLaunch& p, int c) {
 }
 
 template <typename T, typename YT, int W>
-__global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLaunch p) {
+__global__ void __launch_bounds__(kConvThreads, 4) conv_update_kernel(const ConvLaunch p) {
   asm volatile("griddepcontrol.launch_dependents;");
   const int uy = blockIdx.y;
   const int s = uy < p.units0 ? 0 : 1;
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
     n = unit;
     seg = 0;
     if (n >= R.num_seqs) return;
-  } else if (!locate_unit(R, 0, R.num_seqs, kConvSeg, unit, n, seg, p.status)) {
+  } else if (!locate_unit(R, 0, R.num_seqs, kConvSegNS, unit, n, seg, p.status)) {
     return;
   }
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
@@ -102,9 +102,10 @@ __global__ void __launch_bounds__(kConvThreads) conv_update_kernel(const ConvLau
     if (reporter) set_status(p.status, GDN_STATUS_ROW_RANGE);
     return;
   }
-  const int t0 = seg * kConvSeg;
+  const int seg_len = R.is_spec ? kConvSeg : kConvSegNS;
+  const int t0 = seg * seg_len;
   if (t0 >= L) return;
-  const int t1 = min(L, t0 + kConvSeg);
+  const int t1 = min(L, t0 + seg_len);
 
   int slot, anchor;  // the row's conv slot; the history's column offset
   int rd;            // the slot the history is read from

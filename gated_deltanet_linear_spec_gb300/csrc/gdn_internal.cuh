@@ -208,8 +208,10 @@ inline RowsDev rows_dev(const gdn_rows* r) {
   return d;
 }
 
-// Conv: tokens per work unit of a long (non-spec) row.  Spec rows are one unit each.
+// Conv work units: a spec row is one unit of at most kConvSeg tokens; a non-spec row is cut into
+// units of kConvSegNS tokens (short units keep each thread's chain of dependent token loads short).
 constexpr int kConvSeg = 64;
+constexpr int kConvSegNS = 16;
 constexpr int kConvThreads = 128;  // each thread owns 8 channels
 
 struct ConvLaunch {
