@@ -224,3 +224,15 @@ def test_output_alignment_on_the_chunked_path(lib):
     # the tensor-core prefill writes 16-byte output vectors: a misaligned out is refused there
     pre = ns_rows(n=8, t=300)
     assert mixed(lib, non_spec=pre, decodes=6, prefills=2, out=FAKE + 2) == ERR["ALIGN"]
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="relies on validation alone to stop a launch with fake pointers")
+def test_conv_grid_limit_is_checked_before_launch(lib):
+    # non-spec rows are cut into 16-token conv work units (grid.y); ~1.1 M tokens need more than
+    # the 65535 units one launch can address, which must be refused before anything is enqueued
+    layer, prm, pl = big_layer(), params(), pools()
+    big = ns_rows(n=8, t=1_100_000, token_indx=FAKE)
+    assert lib.gdn_conv_update(ctypes.byref(layer), ctypes.byref(prm), ctypes.byref(pl), FAKE, 1_100_000,
+                               ctypes.byref(big), FAKE, gdn.GDN_F32, None, None) == ERR["SHAPE"]
+    assert mixed(lib, non_spec=big, decodes=0, prefills=8) == ERR["SHAPE"]
