@@ -183,6 +183,9 @@ size_t gdn_prefill_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* 
  * other columns and slots are untouched; slot <= 0 is not written; L = 0 rows do nothing.
  *   x [num_global_tokens, C] act dtype (global order, gathered through token_indx);
  *   y [rows->num_tokens, C] in y_dtype (local order).
+ * Size limit: one launch covers at most 65535 work units (a spec row is one unit; a non-spec
+ * subset counts ceil(num_tokens / 16) + num_seqs), else GDN_ERR_SHAPE; gdn_mixed_batch counts
+ * both subsets together.
  */
 int gdn_conv_update(const gdn_layer_desc* layer, const gdn_layer_params* params, const gdn_pools* pools,
                     const void* x, int32_t num_global_tokens, const gdn_rows* rows, void* y,
