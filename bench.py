@@ -51,10 +51,23 @@ WORKLOADS = {
 }
 
 
-def make_workload(name):
+# Seeded index sets the timed steps rotate over (slots, acceptance counts, NULL positions and
+# activations differ; the distributions are the workload's).  The first is the parity workload.
+INDEX_SETS = {"spec_verify": (2, 1002, 2002, 3002), "non_spec_decode": (1, 1001, 2001, 3001),
+              "mixed": (3, 1003, 2003, 3003), "long_prefill": (20,)}
+
+
+def make_workload(name, seed=None):
     from gated_deltanet_linear_spec_gb300 import workloads
+    seed = INDEX_SETS[name][0] if seed is None else seed
     return {"spec_verify": workloads.spec_verify, "non_spec_decode": workloads.non_spec_decode,
-            "mixed": workloads.mixed, "long_prefill": lambda: workloads.long_prefill(8192)}[name]()
+            "mixed": workloads.mixed, "long_prefill": lambda seed: workloads.long_prefill(8192, seed)}[name](seed=seed)
+
+
+def workload_config(args) -> dict:
+    """The workload a line is quoted on: identical keys and values in both arms."""
+    return {"workload": WORKLOADS[args.workload], "index_sets": len(INDEX_SETS[args.workload]),
+            "qkv_layout": args.qkv_layout, "conv_layout": args.conv_layout}
 
 
 def source_hash(*names) -> str:
@@ -142,49 +155,122 @@ def algorithmic_bytes(batch) -> dict:
 # clocks during the timed region
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clocks and clock-event (throttle) reasons sampled during the run, by read-only NVML
+    queries from a background thread every ~1 ms (nvidia-smi's 200 ms polling when the NVML
+    library cannot be loaded).  Nothing here changes a setting of the GPU."""
 
-    def __init__(self, gpu_index: int):
-        self.proc = None
-        self.path = None
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, cuda_index: int, period_s: float = 0.001):
+        import threading
+        self.samples = []  # (perf_counter, sm_mhz, max_mhz, reason names)
+        self.windows = []  # (start, end) of the metric's timed region
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._smi = None
+        dev = self._nvml_device(cuda_index)
+        if dev is not None:
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._nvml_loop, args=(dev, period_s), daemon=True)
+            self._thread.start()
+        else:
+            self._start_smi(cuda_index)
+
+    def _nvml_device(self, cuda_index):
+        import ctypes
         try:
-            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
-            self.fh = os.fdopen(fd, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-i", str(gpu_index), "-lms", "200"], stdout=self.fh,
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            uuid = None
+            try:
+                u = str(torch.cuda.get_device_properties(cuda_index).uuid)
+                uuid = u if u.startswith("GPU-") else "GPU-" + u
+            except Exception:
+                pass
+            if uuid is None or lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(h)) != 0:
+                    return None
+            self._lib = lib
+            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            return h
+        except (OSError, AttributeError):
+            return None
+
+    def _nvml_loop(self, h, period_s):
+        import ctypes
+        sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            ok = self._lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0  # NVML_CLOCK_SM
+            ok = ok and self._lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
+            ok = ok and self._reasons_fn(h, ctypes.byref(rs)) == 0
+            if ok:
+                names = tuple(n for bit, n in self.REASONS.items() if rs.value & bit)
+                self.samples.append((t, float(sm.value), float(mx.value), names))
+            time.sleep(period_s)
+
+    def _start_smi(self, cuda_index):
+        try:
+            fd, self._path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            self._fh = os.fdopen(fd, "w")
+            self._smi = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(cuda_index), "-lms", "200"], stdout=self._fh,
                                          stderr=subprocess.DEVNULL)
+            self._t0 = time.perf_counter()
+            self.source = "nvidia-smi"
         except Exception:
-            self.proc = None
+            self._smi = None
+
+    def mark(self, start: float, end: float) -> None:
+        """Records one timed region (perf_counter times taken after the synchronizes around it)."""
+        self.windows.append((start, end))
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.fh.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(nm)
-        os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+            try:
+                self._lib.nvmlShutdown()
+            except Exception:
+                pass
+        elif self._smi is not None:
+            self._smi.terminate()
+            try:
+                self._smi.wait(timeout=5)
+            except Exception:
+                self._smi.kill()
+            self._fh.close()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            with open(self._path) as f:
+                for i, line in enumerate(f):
+                    parts = [q.strip() for q in line.split(",")]
+                    try:
+                        sm, mx = float(parts[1]), float(parts[2])
+                    except (ValueError, IndexError):
+                        continue
+                    rs = tuple(n for n, v in zip(names, parts[5:9]) if v.lower() == "active")
+                    self.samples.append((self._t0 + 0.2 * i, sm, mx, rs))
+            os.unlink(self._path)
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"], "samples": 0}
+        inside = [s for s in self.samples if any(a <= s[0] <= b for a, b in self.windows)]
+        use = inside if inside else self.samples
+        reasons = sorted({r for s in use for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in use) if use else None,
+                "sm_max_mhz": max(s[2] for s in use) if use else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "samples_whole_run": len(self.samples),
+                "sm_mhz_whole_run": statistics.median(s[1] for s in self.samples) if self.samples else None,
+                "reasons_whole_run": sorted({r for s in self.samples for r in s[3]}),
+                "source": self.source, "period_ms": 1.0 if self.source == "nvml" else 200.0}
 
 
 # ------------------------------------------------------------------------------------------
@@ -192,27 +278,29 @@ class ClockSampler:
 
 def oracle_tokens_per_s(batch, budget_s: float = 12.0, heads=None) -> dict:
     """The CPU oracle as it stands, timed on this host's cores over a bounded sample: the whole
-    workload (or a few v-heads of it, scaled to all heads), repeated until budget_s has passed."""
+    workload (or a few v-heads of it, scaled to all heads), run repeatedly until budget_s has
+    passed (at least 3 runs); the rate is taken from the median run."""
     from tests.oracle_run import np_act, run_oracle
     cores = len(os.sched_getaffinity(0))
     conv_pool, ssm_pool = np_act(batch.conv_pool), np_act(batch.ssm_pool)  # copied once, outside the timing
     Hv = batch.layer.num_v_heads
     frac = 1.0 if heads is None else (heads[1] - heads[0]) / Hv
-    reps, el = 0, 0.0
-    while el < budget_s and reps < 2000:
+    runs = []
+    while (sum(runs) < budget_s or len(runs) < 3) and len(runs) < 2000:
         t0 = time.perf_counter()
         run_oracle(batch, heads=heads, nthreads=cores, conv_pool=conv_pool, ssm_pool=ssm_pool)
-        el += time.perf_counter() - t0
-        reps += 1
+        runs.append(time.perf_counter() - t0)
     what = "all 32 v-heads" if heads is None else f"v-heads {heads[0]}..{heads[1] - 1} of {Hv}, scaled to all"
     # one single-thread pass of the same sample, for the per-core rate
     t0 = time.perf_counter()
     run_oracle(batch, heads=heads, nthreads=1, conv_pool=conv_pool, ssm_pool=ssm_pool)
     one = time.perf_counter() - t0
-    return {"value": reps * batch.num_actual_tokens * frac / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"the full token set ({batch.num_actual_tokens} tokens), {what}, repeated {reps}x: "
-                      f"{el:.1f} s of CPU time on {cores} threads",
-            "single_thread_value": batch.num_actual_tokens * frac / one, "cpu_model": cpu_model()}
+    tokens = batch.num_actual_tokens * frac
+    return {"value": tokens / statistics.median(runs), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the full token set ({batch.num_actual_tokens} tokens), {what}, run {len(runs)}x "
+                      f"({sum(runs):.1f} s on {cores} threads); rate of the median run",
+            "mean_value": tokens * len(runs) / sum(runs),
+            "single_thread_value": tokens / one, "cpu_model": cpu_model()}
 
 
 def cpu_model() -> str:
@@ -275,6 +363,126 @@ def timed(fn, steps, flush, stream):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def timed_rotating(fns, steps, flush, stream):
+    """Per-step milliseconds (CUDA events on the launching stream); step i runs fns[i % len(fns)],
+    and the L2 flush runs between steps, outside the events."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i, (a, b) in enumerate(ev):
+        a.record(stream)
+        fns[i % len(fns)]()
+        b.record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def per_launch_rate(units_per_set, ms):
+    """Units per second over the timed launches: launch i processed units_per_set[i % n]."""
+    n = len(units_per_set)
+    total = sum(units_per_set[i % n] for i in range(len(ms)))
+    return total / (sum(ms) * 1e-3)
+
+
+def end_to_end(db, batch, stream, flush, steps, dist):
+    """The metric through gdn_mixed_batch with the step's inputs copied from pinned host memory
+    and its outputs copied back, the way a serving loop runs it: two device buffer sets share the
+    pools; step i+1's host->device copies and step i-1's device->host read overlap step i's
+    kernels (copies on their own streams, ordered by events; the kernels stay in order on the
+    compute stream, which carries the state from step to step).  Also the serial sequence
+    (copy in, compute, copy out) and the kernels alone back to back without the L2 flush."""
+    from gated_deltanet_linear_spec_gb300.device_batch import to_device
+    host_in = {k: getattr(db, k).cpu().pin_memory() for k in ("x", "a", "b")}
+    idx = []
+    for sub in (db.spec, db.non_spec):
+        if sub is None:
+            continue
+        for k in ("query_start_loc", "token_indx", "state_indices", "has_initial_state", "spec_state_indices",
+                  "num_accepted_tokens"):
+            t = getattr(sub, k)
+            if t is not None:
+                idx.append((t, t.cpu().pin_memory()))
+    host_out = torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
+        sum(h.numel() * h.element_size() for _, h in idx)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k, t in host_in.items():
+            getattr(db, k).copy_(t, non_blocking=True)
+        for dev, host in idx:
+            dev.copy_(host, non_blocking=True)
+        db.run()
+        host_out.copy_(db.out, non_blocking=True)
+
+    serial_ms = statistics.median(timed(e2e_step, max(3, steps // 4), flush, stream))
+
+    db2 = to_device(batch, pools=db.pools)
+    host_of = dict((id(dv), hv) for dv, hv in idx)
+    sets = []
+    for d in (db, db2):
+        pairs = [(getattr(d, k), host_in[k]) for k in ("x", "a", "b")]
+        for sub, hsub in ((d.spec, db.spec), (d.non_spec, db.non_spec)):
+            if sub is None:
+                continue
+            for k in ("query_start_loc", "token_indx", "state_indices", "has_initial_state", "spec_state_indices",
+                      "num_accepted_tokens"):
+                t = getattr(sub, k)
+                if t is not None:
+                    pairs.append((t, host_of[id(getattr(hsub, k))]))
+        sets.append((d, pairs, torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()))
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+
+    def pipelined(n):
+        for i in range(n):
+            b = i % 2
+            d, pairs, hout = sets[b]
+            with torch.cuda.stream(h2d_s):
+                if i >= 2:
+                    h2d_s.wait_event(done[b])  # step i-2 has finished reading this set's inputs
+                for dev, host in pairs:
+                    dev.copy_(host, non_blocking=True)
+                ready[b].record(h2d_s)
+            stream.wait_event(ready[b])
+            if i >= 2:
+                stream.wait_event(drained[b])  # step i-2's outputs have left this set's buffer
+            d.run(stream)
+            done[b].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(done[b])
+                hout.copy_(d.out, non_blocking=True)
+                drained[b].record(d2h_s)
+
+    # the same kernels back to back without the flush, for comparison with the pipelined number
+    for _ in range(3):
+        db.run()
+    torch.cuda.synchronize()
+    n_steady = max(8, steps // 2)
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0e.record(stream)
+    for _ in range(n_steady):
+        db.run()
+    t1e.record(stream)
+    torch.cuda.synchronize()
+    steady_ms = t0e.elapsed_time(t1e) / n_steady
+
+    pipelined(4)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    n_e2e = max(8, steps // 2)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(h2d_s)
+    pipelined(n_e2e)
+    d2h_s.wait_stream(stream)
+    t_end.record(d2h_s)
+    torch.cuda.synchronize()
+    return {"ms_per_step": t_start.elapsed_time(t_end) / n_e2e, "serial_ms_per_step": serial_ms,
+            "device_ms_per_step_no_flush": steady_ms, "h2d": h2d, "d2h": d2h}
+
+
 def run_sweep(args) -> int:
     """The throughput sweep on one GPU: spec verify at drafts in {1, 2, 4} x batch in {1, 8, 64,
     256, 512} over a 2048-slot pool, then the 8192-token chunked prefill.  Each point prints one
@@ -304,20 +512,20 @@ def run_sweep(args) -> int:
             db.run()
             flush.zero_()
         torch.cuda.synchronize()
-        ms = statistics.mean(timed(db.run, steps, flush, stream))
+        ms = statistics.median(timed(db.run, steps, flush, stream))
         rows = db.spec if db.spec is not None else db.non_spec
         y = torch.empty((rows.num_tokens, batch.layer.channels), dtype=torch.float32, device="cuda")
         gdn.gdn_conv_update(db.layer, db.params, db.pools, db.x, rows, y, db.status)
         if d == "prefill":
             ws = torch.empty(gdn.gdn_prefill_workspace_bytes(db.layer, rows, rows.num_seqs), dtype=torch.uint8,
                              device="cuda")
-            k_ms = statistics.mean(timed(lambda: gdn.gdn_chunk_prefill(db.layer, db.params, db.pools, y, db.a, db.b,
+            k_ms = statistics.median(timed(lambda: gdn.gdn_chunk_prefill(db.layer, db.params, db.pools, y, db.a, db.b,
                                                                        rows, db.out, ws, status=db.status),
                                          steps, flush, stream))
             roof = {"kernel": "gdn_chunk_prefill", "bound": "tensor", "unit": "TFLOP/s", "peak": bf16,
                     "achieved": prefill_flops(batch) / (k_ms * 1e-3) / 1e12, "launch_ms": k_ms}
         else:
-            k_ms = statistics.mean(timed(lambda: gdn.gdn_recurrent_step(db.layer, db.params, db.pools, y, db.a, db.b,
+            k_ms = statistics.median(timed(lambda: gdn.gdn_recurrent_step(db.layer, db.params, db.pools, y, db.a, db.b,
                                                                         rows, db.out, db.status),
                                          steps, flush, stream))
             roof = {"kernel": "gdn::recurrent_kernel", "bound": "hbm", "unit": "GB/s", "peak": hbm,
@@ -371,8 +579,8 @@ def main() -> int:
         line = {"metric": METRIC, "value": ref["value"], "unit": UNIT, "n_gpus": 0, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": per_step_s * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": WORKLOADS[args.workload], "qkv_layout": args.qkv_layout,
-                           "conv_layout": args.conv_layout, "parallelism": "host CPU (oracle)"},
+                "config": workload_config(args),
+                "timing": {"where": "host CPU (the oracle, first index set)", "cores": ref["cores"]},
                 "impl": "reference", "cpu_baseline": ref,
                 "e2e": {"value": ref["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -380,6 +588,7 @@ def main() -> int:
 
     import gated_deltanet_linear_spec_gb300 as gdn
     from gated_deltanet_linear_spec_gb300.device_batch import to_device
+    from gated_deltanet_linear_spec_gb300.workloads import with_layouts
 
     torch.cuda.set_device(local_rank)
     dist = None
@@ -387,188 +596,125 @@ def main() -> int:
         import torch.distributed as dist  # noqa: F811
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
 
-    from gated_deltanet_linear_spec_gb300.workloads import with_layouts
-    batch = with_layouts(make_workload(args.workload), qkv_layout=int(args.qkv_layout == "per_khead"),
-                         conv_layout=int(args.conv_layout == "per_slot"))
-    db = to_device(batch)
-    alg = algorithmic_bytes(batch)
+    clocks = ClockSampler(local_rank)
+    batches = [with_layouts(make_workload(args.workload, seed), qkv_layout=int(args.qkv_layout == "per_khead"),
+                            conv_layout=int(args.conv_layout == "per_slot")) for seed in INDEX_SETS[args.workload]]
+    dbs = [to_device(b) for b in batches]
+    algs = [algorithmic_bytes(b) for b in batches]
+    batch, db = batches[0], dbs[0]
     T = batch.num_actual_tokens
+    assert all(b.num_actual_tokens == T for b in batches)
+    nsets = len(dbs)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     steps = args.steps if not big else max(3, args.steps // 40)
 
-    # -------- device-timed steps: the whole path through gdn_mixed_batch, L2 flushed in between
-    for _ in range(args.warmup):
-        db.run()
+    # -------- device-timed steps: the whole path through gdn_mixed_batch, L2 flushed in between,
+    #          step i on index set i % nsets
+    for i in range(args.warmup):
+        dbs[i % nsets].run()
         flush.zero_()
     torch.cuda.synchronize()
-    step_fn = db.run
+    step_fns = [d.run for d in dbs]
     if args.graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            db.run()
-        for _ in range(args.warmup):
-            graph.replay()
+        graphs = []
+        for d in dbs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                d.run()
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % nsets].replay()
             flush.zero_()
         torch.cuda.synchronize()
-        step_fn = graph.replay
-    clocks = ClockSampler(local_rank)
+        step_fns = [g.replay for g in graphs]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    step_ms = timed(step_fn, steps, flush, stream)
+    t_region0 = time.perf_counter()
+    step_ms = timed_rotating(step_fns, steps, flush, stream)
+    torch.cuda.synchronize()
+    clocks.mark(t_region0, time.perf_counter())
     if dist:
         dist.barrier()
 
-    # -------- the dominant kernels alone, through the public entry points that launch them
-    rows = db.spec if db.spec is not None else db.non_spec
-    y = torch.empty((rows.num_tokens, batch.layer.channels), dtype=torch.float32, device="cuda")
-    conv_ms = statistics.mean(timed(lambda: gdn.gdn_conv_update(db.layer, db.params, db.pools, db.x, rows, y,
-                                                                db.status), steps, flush, stream))
+    # -------- the dominant kernel alone, through the public entry point that launches exactly it
+    ys = []
+    for d in dbs:
+        rows = d.spec if d.spec is not None else d.non_spec
+        ys.append(torch.empty((rows.num_tokens, batch.layer.channels), dtype=torch.float32, device="cuda"))
+
+    def conv_fn(d, y):
+        rows = d.spec if d.spec is not None else d.non_spec
+        return lambda: gdn.gdn_conv_update(d.layer, d.params, d.pools, d.x, rows, y, d.status)
+
+    conv_ms = timed_rotating([conv_fn(d, y) for d, y in zip(dbs, ys)], steps, flush, stream)
     if args.workload == "long_prefill":
-        ws = torch.empty(gdn.gdn_prefill_workspace_bytes(db.layer, rows, rows.num_seqs), dtype=torch.uint8,
-                         device="cuda")
-        kern_ms = statistics.mean(timed(lambda: gdn.gdn_chunk_prefill(db.layer, db.params, db.pools, y, db.a, db.b,
-                                                                      rows, db.out, ws, status=db.status),
-                                        steps, flush, stream))
+        def prefill_fn(d, y):
+            rows = d.non_spec
+            ws = torch.empty(gdn.gdn_prefill_workspace_bytes(d.layer, rows, rows.num_seqs), dtype=torch.uint8,
+                             device="cuda")
+            return lambda: gdn.gdn_chunk_prefill(d.layer, d.params, d.pools, y, d.a, d.b, rows, d.out, ws,
+                                                 status=d.status)
+        kern_ms = timed_rotating([prefill_fn(d, y) for d, y in zip(dbs, ys)], steps, flush, stream)
+        flops = [prefill_flops(b) for b in batches]
         peaks = measured_peaks()
         peak = peaks.get("bf16_tflops")
         roof = {"kernel": "gdn chunk_prep_kernel + chunk_scan_kernel (gdn_chunk_prefill)", "bound": "tensor",
-                "achieved": prefill_flops(batch) / (kern_ms * 1e-3) / 1e12, "peak": peak or FALLBACK_BF16_TFLOPS,
-                "peak_source": "measured" if peak else "fallback", "unit": "TFLOP/s", "traffic": None,
-                "algorithmic_flops_per_launch": prefill_flops(batch), "launch_ms": kern_ms, "conv_launch_ms": conv_ms}
+                "achieved": per_launch_rate(flops, kern_ms) / 1e12, "peak": peak or FALLBACK_BF16_TFLOPS,
+                "peak_source": "measured (bf16 burst)" if peak else "fallback", "unit": "TFLOP/s", "traffic": None,
+                "algorithmic_flops_per_launch": statistics.mean(flops), "launch_ms": statistics.median(kern_ms),
+                "launch_ms_mean": statistics.mean(kern_ms), "conv_launch_ms": statistics.median(conv_ms)}
     else:
-        kern_ms = statistics.mean(timed(lambda: gdn.gdn_recurrent_step(db.layer, db.params, db.pools, y, db.a, db.b,
-                                                                       rows, db.out, db.status), steps, flush, stream))
+        def rec_fn(d, y):
+            rows = d.spec if d.spec is not None else d.non_spec
+            return lambda: gdn.gdn_recurrent_step(d.layer, d.params, d.pools, y, d.a, d.b, rows, d.out, d.status)
+        kern_ms = timed_rotating([rec_fn(d, y) for d, y in zip(dbs, ys)], steps, flush, stream)
+        rec_bytes = [a["recurrence"] for a in algs]
         peaks = measured_peaks()
         peak = peaks.get("hbm_gbs")
         src = source_hash("gdn_recurrent.cu", "gdn_internal.cuh")
-        roof = {"kernel": "gdn::recurrent_kernel", "bound": "hbm", "achieved": alg["recurrence"] / (kern_ms * 1e-3) / 1e9,
-                "peak": peak or FALLBACK_HBM_GBS, "peak_source": "measured" if peak else "fallback", "unit": "GB/s",
-                "traffic": recorded_traffic("recurrent_kernel", args.workload, src), "source_hash": src,
-                "algorithmic_bytes_per_launch": alg["recurrence"], "launch_ms": kern_ms, "conv_launch_ms": conv_ms}
+        roof = {"kernel": "gdn::recurrent_kernel", "bound": "hbm", "achieved": per_launch_rate(rec_bytes, kern_ms) / 1e9,
+                "peak": peak or FALLBACK_HBM_GBS, "peak_source": "measured (copy)" if peak else "fallback",
+                "unit": "GB/s", "traffic": recorded_traffic("recurrent_kernel", args.workload, src),
+                "source_hash": src, "algorithmic_bytes_per_launch": statistics.mean(rec_bytes),
+                "launch_ms": statistics.median(kern_ms), "launch_ms_mean": statistics.mean(kern_ms),
+                "conv_launch_ms": statistics.median(conv_ms)}
     roof["frac"] = roof["achieved"] / roof["peak"]
+
+    # -------- end to end: pinned host inputs -> device -> gdn_mixed_batch -> host outputs (set 0)
+    e2e = end_to_end(db, batch, stream, flush, steps, dist)
     clk = clocks.stop()
 
-    # -------- end to end: pinned host inputs -> device -> gdn_mixed_batch -> host outputs
-    host_in = {k: getattr(db, k).cpu().pin_memory() for k in ("x", "a", "b")}
-    idx = []
-    for sub in (db.spec, db.non_spec):
-        if sub is None:
-            continue
-        for k in ("query_start_loc", "token_indx", "state_indices", "has_initial_state", "spec_state_indices",
-                  "num_accepted_tokens"):
-            t = getattr(sub, k)
-            if t is not None:
-                idx.append((t, t.cpu().pin_memory()))
-    host_out = torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
-        sum(h.numel() * h.element_size() for _, h in idx)
-    d2h = host_out.numel() * host_out.element_size()
-
-    def e2e_step():
-        for k, t in host_in.items():
-            getattr(db, k).copy_(t, non_blocking=True)
-        for dev, host in idx:
-            dev.copy_(host, non_blocking=True)
-        db.run()
-        host_out.copy_(db.out, non_blocking=True)
-
-    e2e_serial_ms = statistics.mean(timed(e2e_step, max(3, steps // 4), flush, stream))
-
-    # Pipelined end to end, the way a serving loop runs it: two device buffer sets share the
-    # pools; step i+1's host->device copies and step i-1's device->host read overlap step i's
-    # kernels (copies on their own streams, ordered by events; the kernels stay in order on the
-    # compute stream, which carries the state from step to step).
-    db2 = to_device(batch, pools=db.pools)
-    sets = []
-    for d in (db, db2):
-        pairs = [(getattr(d, k), host_in[k]) for k in ("x", "a", "b")]
-        for sub, hsub in ((d.spec, db.spec), (d.non_spec, db.non_spec)):
-            if sub is None:
-                continue
-            for k in ("query_start_loc", "token_indx", "state_indices", "has_initial_state", "spec_state_indices",
-                      "num_accepted_tokens"):
-                t = getattr(sub, k)
-                if t is not None:
-                    pairs.append((t, dict((id(dv), hv) for dv, hv in idx)[id(getattr(hsub, k))]))
-        sets.append((d, pairs, torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()))
-    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
-    ready = [torch.cuda.Event() for _ in range(2)]
-    done = [torch.cuda.Event() for _ in range(2)]
-    drained = [torch.cuda.Event() for _ in range(2)]
-
-    def e2e_pipelined(n):
-        for i in range(n):
-            b = i % 2
-            d, pairs, hout = sets[b]
-            with torch.cuda.stream(h2d_s):
-                if i >= 2:
-                    h2d_s.wait_event(done[b])  # step i-2 has finished reading this set's inputs
-                for dev, host in pairs:
-                    dev.copy_(host, non_blocking=True)
-                ready[b].record(h2d_s)
-            stream.wait_event(ready[b])
-            if i >= 2:
-                stream.wait_event(drained[b])  # step i-2's outputs have left this set's buffer
-            d.run(stream)
-            done[b].record(stream)
-            with torch.cuda.stream(d2h_s):
-                d2h_s.wait_event(done[b])
-                hout.copy_(d.out, non_blocking=True)
-                drained[b].record(d2h_s)
-
-    # the same kernels back to back without the flush, for comparison with the pipelined number
-    for _ in range(3):
-        db.run()
-    torch.cuda.synchronize()
-    n_steady = max(8, steps // 2)
-    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0e.record(stream)
-    for _ in range(n_steady):
-        db.run()
-    t1e.record(stream)
-    torch.cuda.synchronize()
-    steady_ms = t0e.elapsed_time(t1e) / n_steady
-
-    e2e_pipelined(4)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    n_e2e = max(8, steps // 2)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(h2d_s)
-    e2e_pipelined(n_e2e)
-    d2h_s.wait_stream(stream)
-    t_end.record(d2h_s)
-    torch.cuda.synchronize()
-    e2e_ms = t_start.elapsed_time(t_end) / n_e2e
-
     status = int(db.status.item())
-    ms = statistics.mean(step_ms)
-    ms, e2e_ms, e2e_serial_ms, steady_ms = reduce_max_over_ranks([ms, e2e_ms, e2e_serial_ms, steady_ms], dist,
-                                                                 device="cuda")
+    ms, ms_mean = statistics.median(step_ms), statistics.mean(step_ms)
+    ms, ms_mean, e2e_ms, e2e_serial_ms, steady_ms = reduce_max_over_ranks(
+        [ms, ms_mean, e2e["ms_per_step"], e2e["serial_ms_per_step"], e2e["device_ms_per_step_no_flush"]], dist,
+        device="cuda")
     if rank != 0:
         dist.destroy_process_group()
         return 0
 
     launches_per_step = 2 + (2 if batch.num_prefills and gdn.gdn_prefill_workspace_bytes(
         db.layer, db.non_spec, batch.num_prefills) else 0)
+    alg_total = statistics.mean(a["total"] for a in algs)
     line = {
         "metric": METRIC, "value": job_throughput(T, world, ms), "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOADS[args.workload], "l2": "flushed between steps (512 MiB write)",
+        "config": workload_config(args),
+        "timing": {"statistic": "median over the timed steps", "ms_per_step_mean": ms_mean,
+                   "l2": "flushed between steps (512 MiB write)",
+                   "index_sets": f"step i runs seeded index set i % {nsets} (seeds {list(INDEX_SETS[args.workload])})",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "qkv_layout": args.qkv_layout, "conv_layout": args.conv_layout,
                    "launch": "cuda graph replay" if args.graph else "eager",
-                   "hbm_gbs_whole_step": alg["total"] / (ms * 1e-3) / 1e9,
-                   "algorithmic_bytes_per_step": alg["total"], "status": status},
+                   "hbm_gbs_whole_step": alg_total / (ms * 1e-3) / 1e9,
+                   "algorithmic_bytes_per_step": alg_total, "status": status},
         "roofline": roof,
-        "e2e": {"value": job_throughput(T, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+        "e2e": {"value": job_throughput(T, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e_ms,
                 "mode": "pipelined over steps (copies overlap the previous/next step's kernels; no L2 flush: "
-                        "the state a step touches exceeds L2)",
+                        "the state a step touches exceeds L2); index set 0",
                 "serial_ms_per_step": e2e_serial_ms,
                 "device_ms_per_step_no_flush": steady_ms},
         "gpu_launches": launches_per_step * steps,

@@ -63,6 +63,8 @@ class _Rows(ctypes.Structure):
 
 EXPORTS = ("gdn_workspace_bytes", "gdn_prefill_workspace_bytes", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
            "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "gdn_status_string")
+# include/gdn_testing.h: hooks that let tests drive the kernels' failure paths
+TESTING_EXPORTS = ("gdn_testing_set_prefill_faults",)
 STATIC_WORKSPACE_BYTES = 16 << 20
 
 _lib = None
@@ -99,6 +101,8 @@ def library() -> ctypes.CDLL:
             lib.gdn_mixed_batch_static_workspace.restype = ctypes.c_int
             lib.gdn_mixed_batch_static_workspace.argtypes = [P(_LayerDesc), P(_LayerParams), P(_Pools), VP, VP, VP,
                                                              I32, P(_Rows), I32, I32, P(_Rows), VP, VP, VP]
+            lib.gdn_testing_set_prefill_faults.restype = ctypes.c_int
+            lib.gdn_testing_set_prefill_faults.argtypes = [ctypes.c_uint64, I32]
             _lib = lib
     return _lib
 
@@ -301,7 +305,15 @@ def gdn_mixed_batch_static_workspace(layer: Layer, params: Params, pools: Pools,
     _check(rc)
 
 
+def gdn_testing_set_prefill_faults(wait_ns: int = 0, drop_copy_chunk: int = -1) -> None:
+    """Test hook (include/gdn_testing.h): the wall-clock limit of the chunked prefill's bounded
+    waits (0 = the default, one second) and a chunk whose record copy the scan leaves out on
+    purpose (< 0 = none), for every later prefill launch in this process."""
+    _check(library().gdn_testing_set_prefill_faults(int(wait_ns), int(drop_copy_chunk)))
+
+
 __all__ = ["Layer", "Params", "Pools", "Rows", "GdnError", "library", "LIB_PATH", "EXPORTS",
            "gdn_workspace_bytes", "gdn_prefill_workspace_bytes", "mixed_batch_workspace_bytes", "STATUS_WAIT_TIMEOUT", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
-           "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "STATIC_WORKSPACE_BYTES", "GDN_F32", "GDN_BF16", "STATUS_SLOT_RANGE", "STATUS_NUM_ACCEPTED",
+           "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "STATIC_WORKSPACE_BYTES",
+           "TESTING_EXPORTS", "gdn_testing_set_prefill_faults", "GDN_F32", "GDN_BF16", "STATUS_SLOT_RANGE", "STATUS_NUM_ACCEPTED",
            "STATUS_TOKEN_RANGE", "STATUS_ROW_RANGE"]

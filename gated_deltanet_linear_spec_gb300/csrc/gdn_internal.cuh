@@ -271,7 +271,13 @@ struct PrefillLaunch {
   int32_t num_rows;
   uint8_t* ws;        // units x Hv records of kRecBytes
   uint32_t* status;
+  uint64_t wait_ns;         // wall-clock limit of each bounded mbarrier wait
+  int32_t drop_copy_chunk;  // test hook: the scan issues no record copy for this chunk (< 0: none)
 };
+
+// Default limit of a bounded wait in the tensor-core kernels: far beyond any legitimate wait
+// (a few microseconds), short enough that a lost arrival ends the launch promptly.
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 // Host launchers (one per kernel family); return cudaGetLastError() after the launch.
 cudaError_t launch_conv(const ConvLaunch& p, int width, gdn_dtype act, gdn_dtype y_dtype, int units_total,

@@ -29,6 +29,7 @@
 // TMEM and returns.
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
+#include "gdn_testing.h"
 
 namespace gdn {
 
@@ -88,9 +89,29 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
   x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
 }
 
+// g = -exp(A_log) softplus(a + dt_bias), held at -256 or above: e^g is 0 in fp32 from about
+// -104 on either way, and the floor keeps a chunk's cumulative sum finite (an infinite or NaN g
+// would turn every difference G_t - G_s of the chunk into NaN).
 __device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
   const float x = a + dt_bias;
-  return -expf(A_log) * (x > 20.f ? x : log1pf(expf(x)));
+  return fmaxf(-expf(A_log) * (x > 20.f ? x : log1pf(expf(x))), -256.f);
+}
+
+// Error-free sum: s + e == a + b exactly (Knuth's TwoSum; no operation here may be contracted or
+// reassociated, and nvcc does neither for additions).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// (ah + al) + (bh + bl) as a normalised pair (hi carries the fp32 rounding of the sum).
+__device__ __forceinline__ void add_pair(float ah, float al, float bh, float bl, float& h, float& l) {
+  float s, e;
+  two_sum(ah, bh, s, e);
+  e += al + bl;
+  h = s + e;
+  l = e - (h - s);
 }
 
 // One 16 x 16 block T_ij of T = (I + A)^-1 (i > j), for the NR rows r0 .. r0+NR-1 of column c:
@@ -154,7 +175,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   float* sA = reinterpret_cast<float*>(sm + 81920);  // A [64][kAStride]  (after MMA 1)
   uint8_t* t_hi = sm + 65536;  // T [64][64]
   uint8_t* t_lo = sm + 73728;
-  __shared__ float sG[kCh], sBeta[kCh], sRk[kCh], sBG[kCh];
+  // cumulative log-decay G_t as a pair sG + sGl: after a strongly decaying token G is large
+  // while the later differences G_t - G_s that weight the chunk products stay small, and a single
+  // fp32 sum would lose them to cancellation
+  __shared__ float sG[kCh], sGl[kCh], sBeta[kCh], sRk[kCh], sBG[kCh];
   __shared__ float sMs[3][256];  // per-block 16 x 16 scratch of the blocked solve
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tmem_base;
@@ -198,14 +222,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const uint32_t tmem = tmem_base;
   if (warp == 0) {  // G_t = g_1 + .. + g_t (inclusive): lane l sums tokens 2l, 2l+1, then a warp scan
     const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
-    float x = g0 + g1;
+    float xh, xl;
+    two_sum(g0, g1, xh, xl);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const float yh = __shfl_up_sync(0xffffffffu, xh, o), yl = __shfl_up_sync(0xffffffffu, xl, o);
+      if (lane >= o) add_pair(yh, yl, xh, xl, xh, xl);
     }
-    sG[2 * lane] = x - g1;
-    sG[2 * lane + 1] = x;
+    float eh = __shfl_up_sync(0xffffffffu, xh, 1), el = __shfl_up_sync(0xffffffffu, xl, 1);
+    if (lane == 0) eh = el = 0.f;
+    float h0, l0, h1, l1;
+    add_pair(eh, el, g0, 0.f, h0, l0);
+    add_pair(h0, l0, g1, 0.f, h1, l1);
+    sG[2 * lane] = h0;
+    sGl[2 * lane] = l0;
+    sG[2 * lane + 1] = h1;
+    sGl[2 * lane + 1] = l1;
   }
   __syncthreads();
 
@@ -272,7 +304,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     tc::commit(&bar);
   }
   if (tid < kCh) sBG[tid] = sBeta[tid] * expf(sG[tid]);  // beta_t gamma_t, the row scale of k^ in W
-  bool ok = __syncthreads_and(tc::mbar_wait(&bar, 0));
+  bool ok = __syncthreads_and(tc::mbar_wait(&bar, 0, p.wait_ns));
   if (ok) {
     tc::fence_after();
     // 4. P rows to the record (lane quarters 0, 1: q rows); A rows to shared memory (quarters
@@ -281,7 +313,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     float v0[32];
     tc::tmem_ld32(tc::tmem_lane_col(tmem, quarter, 32 * chalf), v0);
     const int t = (quarter & 1) * 32 + lane;
-    const float Gt = sG[t];
+    const float Gt = sG[t], Gtl = sGl[t];
     if (quarter < 2) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -289,7 +321,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int s = 32 * chalf + 8 * j + e;
-          x[e] = s <= t ? __expf(Gt - sG[s]) * v0[8 * j + e] : 0.f;
+          x[e] = s <= t ? __expf((Gt - sG[s]) + (Gtl - sGl[s])) * v0[8 * j + e] : 0.f;
         }
         *reinterpret_cast<uint4*>(rec + kP + tc::img_off(t, 32 * chalf + 8 * j, 1)) = tc::pack8(x);
       }
@@ -301,7 +333,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int s = 32 * chalf + j + e;
-          x[e] = s < t ? bt * __expf(Gt - sG[s]) * v0[j + e] : 0.f;
+          x[e] = s < t ? bt * __expf((Gt - sG[s]) + (Gtl - sGl[s])) * v0[j + e] : 0.f;
         }
         *reinterpret_cast<float4*>(sA + t * kAStride + 32 * chalf + j) = make_float4(x[0], x[1], x[2], x[3]);
       }
@@ -384,7 +416,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       //     no longer needs, and the k^ rows of the [q^; k^] images scaled in place by
       //     beta_s gamma_s; on the way, the record's K' rows e^{G_c - G_s} k^_s (the same layout).
       //     The v loads are issued first and stay in flight during the k^ pass.
-      const float Gc = sG[kCh - 1];
+      const float Gc = sG[kCh - 1], Gcl = sGl[kCh - 1];
       const int tw0 = (warp - 4) * 16;  // warp 4 + i takes v rows 16i .. 16i+15; lane = 4 dv
       float v[16][4];
 #pragma unroll
@@ -406,7 +438,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         float kn[8], x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) kn[e] = __bfloat162float(hb[e]) + __bfloat162float(lb[e]);
-        const float f = sBG[t], fp = expf(Gc - sG[t]);  // padded tokens: k^ = 0
+        const float f = sBG[t], fp = expf((Gc - sG[t]) + (Gcl - sGl[t]));  // padded tokens: k^ = 0
         uint4 nh, nl;
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = fp * kn[e];
@@ -453,7 +485,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       }
       tc::commit(&bar);
     }
-    ok = __syncthreads_and(tc::mbar_wait(&bar, 1));
+    ok = __syncthreads_and(tc::mbar_wait(&bar, 1, p.wait_ns));
     if (ok) {
       tc::fence_after();
       // 8. -W and U~ (fp32) from TMEM, lane = row d, warp w taking columns 32 (w / 4) .. +31:
@@ -482,8 +514,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   }
   if (!ok) {
     if (tid == 0) set_status(p.status, GDN_STATUS_WAIT_TIMEOUT);
-    tc::mbar_wait(&bar, 0);  // bounded: let any issued MMA drain before TMEM is released
-    tc::mbar_wait(&bar, 1);
+    tc::mbar_wait(&bar, 0, p.wait_ns);  // bounded: let any issued MMA drain before TMEM is released
+    tc::mbar_wait(&bar, 1, p.wait_ns);
   }
   tc::fence_before();
   __syncthreads();
@@ -578,7 +610,11 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
       }
     }
   };
-  auto issue = [&](int c) {  // chunk c's record -> buffer c & 1
+  // chunk c's record -> buffer c & 1 (thread 0).  The test hook drop_copy_chunk leaves one
+  // chunk's copy out, so the wait for it runs out with nothing in flight.
+  auto issued = [&](int c) { return c != p.drop_copy_chunk; };
+  auto issue = [&](int c) {
+    if (!issued(c)) return;
     const uint8_t* rec = p.ws + ((size_t)(base_unit + c) * p.Hv + h) * kRecBytes;
     uint8_t* buf = sm + (c & 1) * kBufBytes;
     uint64_t* bar = &bar_tma[c & 1];
@@ -591,7 +627,8 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     issue(0);
     if (nch > 1) issue(1);
   }
-  int tma_issued[2] = {1, nch > 1 ? 1 : 0}, tma_done[2] = {0, 0};
+  // copies issued into / waited for (successfully) in each buffer, for the drain after a timeout
+  int tma_issued[2] = {issued(0) ? 1 : 0, nch > 1 && issued(1) ? 1 : 0}, tma_done[2] = {0, 0};
   int mma_commits[5] = {0, 0, 0, 0, 0}, mma_done[5] = {0, 0, 0, 0, 0};
 
   // initial state: images of S_0 (unscaled) and gamma_0 S_0^T in TMEM
@@ -599,8 +636,8 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = read_prior ? gS0[(int64_t)j * kD] : 0.f;
   tc::put_mn32_row(s_hi, s_lo, dk, v, 0, 4);
-  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma[0], 0));
-  tma_done[0] = 1;
+  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma[0], 0, p.wait_ns));
+  if (ok) tma_done[0] = 1;
   if (ok) {
     const float g0 = *reinterpret_cast<const float*>(sm + kBufMeta);
 #pragma unroll
@@ -664,8 +701,8 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     }
     // Each warp goes on as soon as U is ready (the issuing thread's warp joins after issuing the
     // output products); the block-wide barrier comes only before the next products are issued.
-    const bool u_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[0], mma_done[0] & 1) &&
-                                                  tc::mbar_wait(&bar_mma[4], mma_done[4] & 1));
+    const bool u_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[0], mma_done[0] & 1, p.wait_ns) &&
+                                                  tc::mbar_wait(&bar_mma[4], mma_done[4] & 1, p.wait_ns));
     ++mma_done[0];
     ++mma_done[4];
     // U += U~; U^T images (row = dv, column = t)
@@ -716,8 +753,8 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     ++mma_commits[2];
     // the state images are rewritten below: the state products and the first output half (which
     // read them) must be done
-    const bool s_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[1], mma_done[1] & 1) &&
-                                                  tc::mbar_wait(&bar_mma[3], mma_done[3] & 1));
+    const bool s_ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar_mma[1], mma_done[1] & 1, p.wait_ns) &&
+                                                  tc::mbar_wait(&bar_mma[3], mma_done[3] & 1, p.wait_ns));
     ++mma_done[1];
     ++mma_done[3];
     bool tma_ok = true;
@@ -728,8 +765,8 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
       tc::tmem_ld32(tc::tmem_lane_col(tS, warp, 0), v);
       if (c + 1 < nch) {
         const int nb = (c + 1) & 1;
-        tma_ok = tc::mbar_wait(&bar_tma[nb], tma_done[nb] & 1);
-        ++tma_done[nb];
+        tma_ok = tc::mbar_wait(&bar_tma[nb], tma_done[nb] & 1, p.wait_ns);
+        if (tma_ok) ++tma_done[nb];
         const float gn = *reinterpret_cast<const float*>(sm + nb * kBufBytes + kBufMeta);
         float sv[32];
 #pragma unroll
@@ -741,7 +778,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
         for (int j = 0; j < 32; ++j) gS[(int64_t)j * kD] = v[j];
       }
     }
-    const bool mma_ok = s_ok && tc::mbar_wait(&bar_mma[2], mma_done[2] & 1);
+    const bool mma_ok = s_ok && tc::mbar_wait(&bar_mma[2], mma_done[2] & 1, p.wait_ns);
     ok = __syncthreads_and(tma_ok && mma_ok);
     ++mma_done[2];
     if (!ok) break;
@@ -749,7 +786,7 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     if (tid == 0 && c + 2 < nch) {  // this buffer is consumed: fetch chunk c + 2 into it
       issue(c + 2);
     }
-    if (c + 2 < nch) ++tma_issued[b];
+    if (c + 2 < nch && issued(c + 2)) ++tma_issued[b];
     if (c + 1 == nch) store_outputs(c);
     tc::tmem_st_wait();
     tc::fence_async_smem();
@@ -762,9 +799,12 @@ __global__ void __launch_bounds__(128, 1) chunk_scan_kernel(const PrefillLaunch 
     // bounded drains of anything still in flight (the wait that failed included) before TMEM
     // and shared memory are released
     for (int i = 0; i < 5; ++i)
-      for (int k = mma_done[i] > 0 ? mma_done[i] - 1 : 0; k < mma_commits[i]; ++k) tc::mbar_wait(&bar_mma[i], k & 1);
+      for (int k = mma_done[i] > 0 ? mma_done[i] - 1 : 0; k < mma_commits[i]; ++k)
+        tc::mbar_wait(&bar_mma[i], k & 1, p.wait_ns);
+    // copies: only those issued and not yet seen complete (a copy the test hook left out is
+    // neither, so nothing waits for it again)
     for (int bb = 0; bb < 2; ++bb)
-      for (int k = tma_done[bb] > 0 ? tma_done[bb] - 1 : 0; k < tma_issued[bb]; ++k) tc::mbar_wait(&bar_tma[bb], k & 1);
+      for (int k = tma_done[bb]; k < tma_issued[bb]; ++k) tc::mbar_wait(&bar_tma[bb], k & 1, p.wait_ns);
   }
   tc::fence_before();
   __syncthreads();
@@ -784,12 +824,22 @@ cudaError_t launch_prep(const PrefillLaunch& p, int units, cudaStream_t s) {
 
 }  // namespace
 
+namespace {
+// Test hooks (gdn_testing.h): a shorter wait limit and a record copy left out on purpose.
+std::atomic<uint64_t> g_test_wait_ns{0};
+std::atomic<int32_t> g_test_drop_chunk{-1};
+}  // namespace
+
 bool prefill_tc_supported(const gdn_layer_desc* d) {
   return d->head_k_dim == kD && d->head_v_dim == kD && d->act_dtype == GDN_BF16;
 }
 
-cudaError_t launch_prefill(const PrefillLaunch& p, gdn_dtype qkv_dtype, int units_upper, cudaStream_t s) {
-  if (p.num_rows <= 0 || units_upper <= 0) return cudaSuccess;
+cudaError_t launch_prefill(const PrefillLaunch& args, gdn_dtype qkv_dtype, int units_upper, cudaStream_t s) {
+  if (args.num_rows <= 0 || units_upper <= 0) return cudaSuccess;
+  PrefillLaunch p = args;
+  const uint64_t wait = g_test_wait_ns.load(std::memory_order_relaxed);
+  p.wait_ns = wait ? wait : kDefaultWaitNs;
+  p.drop_copy_chunk = g_test_drop_chunk.load(std::memory_order_relaxed);
   cudaError_t e = qkv_dtype == GDN_F32 ? launch_prep<float>(p, units_upper, s) : launch_prep<__nv_bfloat16>(p, units_upper, s);
   if (e != cudaSuccess) return e;
   static std::atomic<uint64_t> configured{0};
@@ -802,3 +852,9 @@ cudaError_t launch_prefill(const PrefillLaunch& p, gdn_dtype qkv_dtype, int unit
 }
 
 }  // namespace gdn
+
+extern "C" int gdn_testing_set_prefill_faults(uint64_t wait_ns, int32_t drop_copy_chunk) {
+  gdn::g_test_wait_ns.store(wait_ns, std::memory_order_relaxed);
+  gdn::g_test_drop_chunk.store(drop_copy_chunk < 0 ? -1 : drop_copy_chunk, std::memory_order_relaxed);
+  return GDN_OK;
+}

@@ -41,14 +41,17 @@ namespace gdn {
 #define GDN_REC_ST_HINT 1  // 0: default store; 1: streaming (.cs) store, evict-first in L2
 #endif
 
+// Streaming 128-bit load of the prior state.  Not the non-coherent (.nc) path: the launch may
+// store to the slot it loads from (spec rows store token num_accepted-1's state there), and .nc
+// is only defined for data that stays unwritten for the kernel's lifetime.
 __device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
   float4 v;
 #if GDN_REC_LD_HINT == 1
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p));
 #else
-  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p));
 #endif

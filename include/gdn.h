@@ -151,15 +151,23 @@ typedef struct {
 
 /*
  * Bytes of device workspace gdn_mixed_batch needs for a batch without prefill rows (non_spec
- * and spec as they will be passed; either may be NULL): the fp32 post-conv q|k|v of every token.
+ * and spec as they will be passed; either may be NULL): the fp32 post-conv q|k|v of every token,
+ * spec subset first, each part rounded up to 256 bytes.  The pages stage the conv output of a
+ * step in a buffer between the conv and the recurrence ("[GDN] Spec-decoding-aware attention
+ * kernel", Changes: causal_conv1d pass 1 writes its outputs for the gated-delta-rule kernel);
+ * keeping it in fp32 rather than the activation dtype is this library's reading (a bf16 rounding
+ * of the post-conv values moves the state by more than the 1e-4 the path is held to).
  * Depends only on the host-side counts in the descriptors.  Returns 0 for invalid descriptors.
  */
 size_t gdn_workspace_bytes(const gdn_layer_desc* layer, const gdn_rows* non_spec, const gdn_rows* spec);
 
 /*
  * Extra workspace the chunked prefill needs when `rows` (a non-spec subset) holds num_prefills
- * prefill rows: one record per (64-token chunk, v-head), bounded from rows->num_tokens and
- * num_prefills.  gdn_mixed_batch needs gdn_workspace_bytes() + gdn_prefill_workspace_bytes(
+ * prefill rows: one record of 123904 bytes per (64-token chunk, v-head), the chunk count bounded
+ * from rows->num_tokens and num_prefills (ceil(num_tokens / 64) + num_prefills).  The pages run
+ * prefill rows through a chunked kernel ("[XE2] Support MTP of QWEN model", Copilot overview:
+ * chunk gated delta rule); the record holds that chunk form's state-independent terms, which
+ * one kernel computes for all chunks at once and the chunk-by-chunk scan reads.  gdn_mixed_batch needs gdn_workspace_bytes() + gdn_prefill_workspace_bytes(
  * layer, non_spec, num_prefills); gdn_chunk_prefill needs gdn_prefill_workspace_bytes(layer,
  * rows, rows->num_seqs).  0 when the layer does not take the tensor-core path (see
  * gdn_chunk_prefill) or num_prefills is 0.
@@ -252,17 +260,24 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
  * memory: a plain C host or a plugin whose framework owns every device allocation and offers
  * no hook for scratch, or a serving loop that must not call cudaMalloc/cudaFree because they
  * can synchronise the device and stall other streams.  The scratch is a fixed device array of
- * GDN_STATIC_WORKSPACE_BYTES inside the library (16 MiB: 512 tokens of an 8192-channel layer):
+ * GDN_STATIC_WORKSPACE_BYTES (16 MiB) inside the library:
+ *   - a batch fits when gdn_workspace_bytes(layer, non_spec, spec) +
+ *     gdn_prefill_workspace_bytes(layer, non_spec, num_prefills) is at most 16 MiB.  Without
+ *     chunked prefill rows that is 512 tokens of an 8192-channel layer; a prefill row on the
+ *     tensor-core path also needs one 123904-byte record per (64-token chunk, v-head), about
+ *     3.8 MiB per chunk at 32 v-heads, so on that layer a batch holds prefill rows of a few
+ *     chunks at most (one 130-token row is already refused);
  *   - it is reserved on every GPU that loads it and stays reserved until the process exits;
  *   - every call on a device shares it, so calls that may overlap on the GPU race on it;
  *   - it keeps the previous call's contents and is never cleared: no scratch element needs to
  *     start at zero, every element a call reads is written earlier by the same call;
- *   - the first call on each device looks up the array's device address with that device
- *     current (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - the first call in each CUDA context (the device's primary context, normally) looks up the
+ *     array's device address with that device current (cudaGetSymbolAddress); make that first
+ *     call before any stream capture, and do not use this entry point across cudaDeviceReset.
  * The caller still passes inputs and outputs exactly as for gdn_mixed_batch.  Returns
- * GDN_ERR_WORKSPACE when gdn_workspace_bytes(layer, non_spec, spec) is larger than
- * GDN_STATIC_WORKSPACE_BYTES, GDN_ERR_CUDA when the address lookup fails, and otherwise what
- * gdn_mixed_batch returns for the same arguments.  The paper has no counterpart to this entry point.
+ * GDN_ERR_WORKSPACE when the batch does not fit (nothing is enqueued), GDN_ERR_CUDA when the
+ * address lookup fails, and otherwise what gdn_mixed_batch returns for the same arguments.
+ * The paper has no counterpart to this entry point.
  */
 #define GDN_STATIC_WORKSPACE_BYTES (16u << 20)
 int gdn_mixed_batch_static_workspace(const gdn_layer_desc* layer, const gdn_layer_params* params,

@@ -16,7 +16,9 @@ import pytest
 import gated_deltanet_linear_spec_gb300 as gdn
 from gated_deltanet_linear_spec_gb300 import _LayerDesc, _LayerParams, _Pools, _Rows
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gdn.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "gdn.h")
+TESTING_HEADER = os.path.join(INCLUDE, "gdn_testing.h")
 FAKE = 0x100000  # an aligned non-NULL address; never dereferenced because validation fails first
 
 
@@ -28,8 +30,8 @@ def lib():
     return gdn.library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(gdn_\w+)\s*\(", text)))
 
@@ -40,6 +42,20 @@ def test_every_declared_function_is_exported(lib):
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
     assert set(gdn.EXPORTS) == set(names)
+
+
+def test_every_header_is_covered_and_exported(lib):
+    headers = sorted(f for f in os.listdir(INCLUDE) if f.endswith(".h"))
+    assert headers == ["gdn.h", "gdn_testing.h"]
+    testing = declared_functions(TESTING_HEADER)
+    assert set(testing) == set(gdn.TESTING_EXPORTS)
+    assert not [n for n in testing if not hasattr(lib, n)]
+
+
+def test_testing_hook_sets_and_resets_without_a_gpu(lib):
+    # host-only: the hook stores settings that later prefill launches read
+    assert lib.gdn_testing_set_prefill_faults(ctypes.c_uint64(10_000_000), 0) == 0
+    assert lib.gdn_testing_set_prefill_faults(ctypes.c_uint64(0), -1) == 0
 
 
 def big_layer(**kw):

@@ -70,3 +70,45 @@ def test_static_workspace_rejects_a_batch_that_does_not_fit():
     assert e.value.name == "WORKSPACE"
     torch.cuda.synchronize()
     assert torch.equal(d.out, before)
+
+
+def test_static_workspace_with_chunked_prefill_rows_matches_mixed_batch():
+    # a small bf16 layer (dk = dv = 128, so prefill rows take the tensor-core path and their
+    # chunk records live in the fixed array too): decode, spec and prefill rows of 70 and 130
+    batch = W.mixed_small()
+    ref = to_device(batch)
+    stat = to_device(batch)
+    need = gdn.gdn_workspace_bytes(stat.layer, stat.non_spec, stat.spec) + \
+        gdn.gdn_prefill_workspace_bytes(stat.layer, stat.non_spec, stat.num_prefills)
+    assert gdn.gdn_prefill_workspace_bytes(stat.layer, stat.non_spec, stat.num_prefills) > 0
+    assert need <= gdn.STATIC_WORKSPACE_BYTES
+    for call in range(2):
+        if call == 1:
+            x, a, b, na = _next_step_inputs(ref, seed=98)
+            for d in (ref, stat):
+                d.x.copy_(x); d.a.copy_(a); d.b.copy_(b); d.spec.num_accepted_tokens.copy_(na)
+        ref.run()
+        gdn.gdn_mixed_batch_static_workspace(stat.layer, stat.params, stat.pools, stat.x, stat.a, stat.b,
+                                             stat.non_spec, stat.num_decodes, stat.num_prefills, stat.spec,
+                                             stat.out, stat.status)
+        torch.cuda.synchronize()
+        assert int(stat.status.item()) == 0 and int(ref.status.item()) == 0
+        _assert_close(stat.out, ref.out, stat.pools.ssm_pool, ref.pools.ssm_pool,
+                      stat.pools.conv_pool, ref.pools.conv_pool)
+
+
+def test_static_workspace_counts_the_prefill_records():
+    # one 130-token prefill row of the 8192-channel layer: its post-conv scratch (4.3 MB) fits,
+    # but with its three chunks of 32 records (15.9 MB) the batch does not
+    batch = W.build_batch(W.big_layer(3), [W.RowSpec("prefill", 130)], num_slots=4, seed=12)
+    d = to_device(batch)
+    base = gdn.gdn_workspace_bytes(d.layer, d.non_spec, d.spec)
+    assert base <= gdn.STATIC_WORKSPACE_BYTES
+    assert base + gdn.gdn_prefill_workspace_bytes(d.layer, d.non_spec, d.num_prefills) > gdn.STATIC_WORKSPACE_BYTES
+    out0, ssm0, conv0 = d.out.clone(), d.pools.ssm_pool.clone(), d.pools.conv_pool.clone()
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_mixed_batch_static_workspace(d.layer, d.params, d.pools, d.x, d.a, d.b, d.non_spec, d.num_decodes,
+                                             d.num_prefills, d.spec, d.out, d.status)
+    assert e.value.name == "WORKSPACE"
+    torch.cuda.synchronize()
+    assert torch.equal(d.out, out0) and torch.equal(d.pools.ssm_pool, ssm0) and torch.equal(d.pools.conv_pool, conv0)
