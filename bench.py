@@ -377,10 +377,10 @@ def timed_rotating(fns, steps, flush, stream):
 
 
 def per_launch_rate(units_per_set, ms):
-    """Units per second over the timed launches: launch i processed units_per_set[i % n]."""
+    """Median over the timed launches of each launch's rate (launch i processed
+    units_per_set[i % n] units in ms[i] milliseconds), in units per second."""
     n = len(units_per_set)
-    total = sum(units_per_set[i % n] for i in range(len(ms)))
-    return total / (sum(ms) * 1e-3)
+    return statistics.median(units_per_set[i % n] / (ms[i] * 1e-3) for i in range(len(ms)))
 
 
 def end_to_end(db, batch, stream, flush, steps, dist):
@@ -472,7 +472,7 @@ def end_to_end(db, batch, stream, flush, steps, dist):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    n_e2e = max(8, steps // 2)
+    n_e2e = max(64, steps // 2)  # long enough that the pipeline's fill and drain do not count
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(h2d_s)
     pipelined(n_e2e)
