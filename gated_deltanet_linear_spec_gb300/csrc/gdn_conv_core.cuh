@@ -1,4 +1,4 @@
-// gdn_conv_core.cuh -- one thread's share of the causal conv1d update: 8 channels of one row.
+// gdn_conv_core.cuh -- one thread's share of the causal conv1d update: VE channels of one row.
 //
 // Semantics ("[GDN] Spec-decoding-aware attention kernel", Problem and Changes: the conv ring is
 // a rolled history in column 0 of the row's slots, read at offset num_accepted-1; token t of a
@@ -12,7 +12,7 @@
 //   from spec_state_indices[n, num_accepted-1] at offset 0, and after token t the last W-1
 //   inputs go to columns 0..W-2 of spec_state_indices[n, t].
 //
-// The thread that reads a slot's history for its 8 channels is the only one that ever writes
+// The thread that reads a slot's history for its VE channels is the only one that ever writes
 // those slot elements, and it writes them only after its reads, so the roll needs no staging
 // buffer and no second pass.  Two kernels use this: the conv kernel (y to global memory) and the
 // fused verify kernel (y to shared memory, one token batch at a time).
@@ -22,13 +22,86 @@
 
 namespace gdn {
 
+// VE consecutive elements of type T as raw 32-bit words (bit-exact copies), moved with the
+// widest vector access their size allows: 16-byte accesses when the size is a multiple of 16
+// bytes, else 8-byte, else 4-byte ones (the callers' offsets are aligned to the access size).
+template <typename T, int VE>
+struct RawV {
+  static constexpr int NW = VE * (int)sizeof(T) / 4;
+  static_assert(NW >= 1 && VE * (int)sizeof(T) % 4 == 0, "whole 32-bit words");
+  uint32_t w[NW];
+};
+
+template <typename T, int VE>
+__device__ __forceinline__ RawV<T, VE> load_rawv(const T* p) {
+  RawV<T, VE> r;
+  constexpr int NW = RawV<T, VE>::NW;
+  if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW / 4; ++i) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + i);
+      r.w[4 * i] = v.x; r.w[4 * i + 1] = v.y; r.w[4 * i + 2] = v.z; r.w[4 * i + 3] = v.w;
+    }
+  } else if constexpr (NW % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW / 2; ++i) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(p) + i);
+      r.w[2 * i] = v.x; r.w[2 * i + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) r.w[i] = __ldg(reinterpret_cast<const unsigned int*>(p) + i);
+  }
+  return r;
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ RawV<T, VE> zero_rawv() {
+  RawV<T, VE> r;
+#pragma unroll
+  for (int i = 0; i < RawV<T, VE>::NW; ++i) r.w[i] = 0u;
+  return r;
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ void store_rawv(T* p, const RawV<T, VE>& r) {
+  constexpr int NW = RawV<T, VE>::NW;
+  if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW / 4; ++i)
+      reinterpret_cast<uint4*>(p)[i] = make_uint4(r.w[4 * i], r.w[4 * i + 1], r.w[4 * i + 2], r.w[4 * i + 3]);
+  } else if constexpr (NW % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW / 2; ++i) reinterpret_cast<uint2*>(p)[i] = make_uint2(r.w[2 * i], r.w[2 * i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) reinterpret_cast<unsigned int*>(p)[i] = r.w[i];
+  }
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ void rawv_to_f32(const RawV<T, VE>& r, float (&f)[VE]) {
+  const T* e = reinterpret_cast<const T*>(&r.w[0]);
+#pragma unroll
+  for (int i = 0; i < VE; ++i) f[i] = to_f32(e[i]);
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ void store_f32v(T* p, const float (&f)[VE]) {
+  RawV<T, VE> r;
+  T* e = reinterpret_cast<T*>(&r.w[0]);
+#pragma unroll
+  for (int i = 0; i < VE; ++i) e[i] = from_f32<T>(f[i]);
+  store_rawv<T, VE>(p, r);
+}
+
 // SiLU(x) = x / (1 + e^-x) with the hardware exponential and fast division: a few ulp of fp32,
 // far inside what the path's tolerances allow, at a fraction of the IEEE cost.  For x < -88 the
 // exponential overflows and the quotient is -0.
 __device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 // Position in x of packed channel c: the identity for the packed layout; for the per-k-head
-// layout, k-head g's group holds q_g, k_g and the v of its Hv/Hk v-heads.  A thread's 8 channels
+// layout, k-head g's group holds q_g, k_g and the v of its Hv/Hk v-heads.  A thread's channels
 // never straddle a head, so they stay contiguous in x.
 __device__ __forceinline__ int64_t x_channel(const ConvLaunch& p, int c) {
   if (p.qkv_layout == GDN_QKV_PACKED) return c;
@@ -58,37 +131,33 @@ __device__ __forceinline__ ConvRow conv_row(const RowsDev& R, int n) {
   return r;
 }
 
-template <typename T, int W>
+template <typename T, int W, int VE>
 struct ConvThread {
-  float w[W][8], bias[8];
-  Raw8<T> win[W - 1];  // raw inputs of the W-1 tokens before the next one
-  int64_t xc;          // where the thread's 8 channels sit in a row of x
+  float w[W][VE], bias[VE];
+  RawV<T, VE> win[W - 1];  // raw inputs of the W-1 tokens before the next one
+  int64_t xc;              // where the thread's VE channels sit in a row of x
   int64_t slot_base;   // pool offset of the row's slot, at the thread's channels
   int c0;
   int slot;            // the row's conv slot (0 when it must not be written)
   bool per_slot, spec_ring, writer;
 
-  // Weights and bias of channels c0 .. c0+7: 8*W contiguous elements, 16-byte vectors.
+  // Weights and bias of channels c0 .. c0+VE-1: VE*W contiguous elements.
   __device__ __forceinline__ void load_params(const ConvLaunch& p, int c) {
     c0 = c;
-    constexpr int NW = 8 * W * (int)sizeof(T) / 16;
-    uint4 wv[NW];
-    const uint4* wsrc = reinterpret_cast<const uint4*>(static_cast<const T*>(p.w) + (int64_t)c0 * W);
+    const RawV<T, VE * W> wv = load_rawv<T, VE * W>(static_cast<const T*>(p.w) + (int64_t)c0 * W);
+    const T* we = reinterpret_cast<const T*>(&wv.w[0]);
 #pragma unroll
-    for (int i = 0; i < NW; ++i) wv[i] = __ldg(wsrc + i);
-    const T* we = reinterpret_cast<const T*>(wv);
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
+    for (int e = 0; e < VE; ++e)
 #pragma unroll
       for (int i = 0; i < W; ++i) w[i][e] = to_f32(we[e * W + i]);
     if (p.bias) {
-      float bb[8];
-      raw8_to_f32(load_raw8(static_cast<const T*>(p.bias) + c0), bb);
+      float bb[VE];
+      rawv_to_f32(load_rawv<T, VE>(static_cast<const T*>(p.bias) + c0), bb);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) bias[e] = bb[e];
+      for (int e = 0; e < VE; ++e) bias[e] = bb[e];
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) bias[e] = 0.f;
+      for (int e = 0; e < VE; ++e) bias[e] = 0.f;
     }
   }
 
@@ -134,10 +203,10 @@ struct ConvThread {
 #pragma unroll
     for (int i = 0; i < W - 1; ++i) {
       if (seg == 0) {
-        win[i] = read_prior ? load_raw8(pool + hist_base + (int64_t)(anchor + i) * C) : zero_raw8<T>();
+        win[i] = read_prior ? load_rawv<T, VE>(pool + hist_base + (int64_t)(anchor + i) * C) : zero_rawv<T, VE>();
       } else {
         const int g = global_token(R, row.bos + t0 - (W - 1) + i, p.num_global, p.status);
-        win[i] = g >= 0 ? load_raw8(x + (int64_t)g * C + xc) : zero_raw8<T>();
+        win[i] = g >= 0 ? load_rawv<T, VE>(x + (int64_t)g * C + xc) : zero_rawv<T, VE>();
       }
     }
     // From here on this thread owns its slot elements: every read of them is done.
@@ -146,12 +215,12 @@ struct ConvThread {
     if (spec_ring) {
       // spec: columns 0..W-3 <- H[1..W-2] (the shifted history); token t goes to column W-2+t.
 #pragma unroll
-      for (int j = 0; j < W - 2; ++j) store_raw8(pool + slot_base + (int64_t)j * C, win[j + 1]);
+      for (int j = 0; j < W - 2; ++j) store_rawv<T, VE>(pool + slot_base + (int64_t)j * C, win[j + 1]);
     }
     return true;
   }
 
-  // Tokens [ta, tb) of the row: y_t (fp32) handed to sink(t, y[8]); the ring columns or per-slot
+  // Tokens [ta, tb) of the row: y_t (fp32) handed to sink(t, y[VE]); the ring columns or per-slot
   // snapshots of those tokens written as they pass.  The x loads of 4 tokens go out together.
   template <typename Sink>
   __device__ __forceinline__ void tokens(const ConvLaunch& p, const RowsDev& R, int n, const ConvRow& row, int ta,
@@ -164,19 +233,19 @@ struct ConvThread {
       int gt[G];
 #pragma unroll
       for (int k = 0; k < G; ++k) gt[k] = (tg + k < tb) ? global_token(R, row.bos + tg + k, p.num_global, p.status) : -1;
-      Raw8<T> xr[G];
+      RawV<T, VE> xr[G];
 #pragma unroll
-      for (int k = 0; k < G; ++k) xr[k] = gt[k] >= 0 ? load_raw8(x + (int64_t)gt[k] * C + xc) : zero_raw8<T>();
+      for (int k = 0; k < G; ++k) xr[k] = gt[k] >= 0 ? load_rawv<T, VE>(x + (int64_t)gt[k] * C + xc) : zero_rawv<T, VE>();
 #pragma unroll
       for (int k = 0; k < G; ++k) {
         const int t = tg + k;
         if (t >= tb) break;
-        float hf[W - 1][8], xf[8], out[8];
+        float hf[W - 1][VE], xf[VE], out[VE];
 #pragma unroll
-        for (int i = 0; i < W - 1; ++i) raw8_to_f32(win[i], hf[i]);
-        raw8_to_f32(xr[k], xf);
+        for (int i = 0; i < W - 1; ++i) rawv_to_f32(win[i], hf[i]);
+        rawv_to_f32(xr[k], xf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < VE; ++e) {
           float acc = bias[e];
 #pragma unroll
           for (int i = 0; i < W - 1; ++i) acc = fmaf(w[i][e], hf[i][e], acc);
@@ -184,7 +253,7 @@ struct ConvThread {
           out[e] = silu(acc);
         }
         sink(t, out);
-        if (spec_ring) store_raw8(pool + slot_base + (int64_t)(W - 2 + t) * C, xr[k]);
+        if (spec_ring) store_rawv<T, VE>(pool + slot_base + (int64_t)(W - 2 + t) * C, xr[k]);
 #pragma unroll
         for (int i = 0; i < W - 2; ++i) win[i] = win[i + 1];
         win[W - 2] = xr[k];
@@ -195,7 +264,7 @@ struct ConvThread {
           } else if (ss > 0) {
             T* dst = pool + (int64_t)ss * p.state_len * C + c0;
 #pragma unroll
-            for (int j = 0; j < W - 1; ++j) store_raw8(dst + (int64_t)j * C, win[j]);
+            for (int j = 0; j < W - 1; ++j) store_rawv<T, VE>(dst + (int64_t)j * C, win[j]);
           }
         }
       }
@@ -211,13 +280,13 @@ struct ConvThread {
     const int L = row.eos - row.bos;
     if (saw_end) {
 #pragma unroll
-      for (int j = 0; j < W - 1; ++j) store_raw8(pool + slot_base + (int64_t)j * C, win[j]);
+      for (int j = 0; j < W - 1; ++j) store_rawv<T, VE>(pool + slot_base + (int64_t)j * C, win[j]);
     } else {
       const T* __restrict__ x = static_cast<const T*>(p.x);
 #pragma unroll
       for (int j = 0; j < W - 1; ++j) {
         const int g = global_token(R, row.bos + L - (W - 1) + j, p.num_global, p.status);
-        store_raw8(pool + slot_base + (int64_t)j * C, g >= 0 ? load_raw8(x + (int64_t)g * C + xc) : zero_raw8<T>());
+        store_rawv<T, VE>(pool + slot_base + (int64_t)j * C, g >= 0 ? load_rawv<T, VE>(x + (int64_t)g * C + xc) : zero_rawv<T, VE>());
       }
     }
   }
