@@ -98,18 +98,6 @@ def recorded_traffic(kernel: str, workload: str, src_hash: str):
     return None
 
 
-def fused_step(batch) -> bool:
-    """Whether gdn_mixed_batch runs this batch as the one fused verify launch: the library takes
-    spec and decode rows through it for dk = 128, dv a multiple of 32 and (dv / 32) * (Hv / Hk)
-    in {4, 8}, and here no prefill row needs the chunked kernels (the library's own rule,
-    restated for the bench's launch count and roofline)."""
-    L = batch.layer
-    nc = (L.head_v_dim // 32) * (L.num_v_heads // L.num_k_heads) if L.head_v_dim % 32 == 0 else 0
-    chunked_prefill = batch.num_prefills > 0 and L.act_dtype == torch.bfloat16 and L.head_k_dim == 128 \
-        and L.head_v_dim == 128
-    return L.head_k_dim == 128 and nc in (4, 8) and not chunked_prefill
-
-
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -495,6 +483,21 @@ def end_to_end(db, batch, stream, flush, steps, dist):
             "device_ms_per_step_no_flush": steady_ms, "h2d": h2d, "d2h": d2h}
 
 
+def run_profile(args) -> int:
+    """The step of the chosen workload, warmup + steps times back to back on its first index set
+    (one pool: the smallest device footprint a profiler has to save and restore)."""
+    from gated_deltanet_linear_spec_gb300.device_batch import to_device
+    from gated_deltanet_linear_spec_gb300.workloads import with_layouts
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    batch = with_layouts(make_workload(args.workload), qkv_layout=int(args.qkv_layout == "per_khead"),
+                         conv_layout=int(args.conv_layout == "per_slot"))
+    db = to_device(batch)
+    for _ in range(args.warmup + args.steps):
+        db.run()
+    torch.cuda.synchronize()
+    return int(db.status.item() != 0)
+
+
 def run_sweep(args) -> int:
     """The throughput sweep on one GPU: spec verify at drafts in {1, 2, 4} x batch in {1, 8, 64,
     256, 512} over a 2048-slot pool, then the 8192-token chunked prefill.  Each point prints one
@@ -536,10 +539,6 @@ def run_sweep(args) -> int:
                                          steps, flush, stream))
             roof = {"kernel": "gdn_chunk_prefill", "bound": "tensor", "unit": "TFLOP/s", "peak": bf16,
                     "achieved": prefill_flops(batch) / (k_ms * 1e-3) / 1e12, "launch_ms": k_ms}
-        elif fused_step(batch):  # the step is the one fused launch
-            roof = {"kernel": "gdn::recurrent_kernel, fused conv (the whole step)", "bound": "hbm", "unit": "GB/s",
-                    "peak": hbm, "achieved": alg["total"] / (ms * 1e-3) / 1e9, "launch_ms": ms,
-                    "algorithmic_bytes_per_launch": alg["total"]}
         else:
             k_ms = statistics.median(timed(lambda: gdn.gdn_recurrent_step(db.layer, db.params, db.pools, y, db.a, db.b,
                                                                         rows, db.out, db.status),
@@ -575,10 +574,14 @@ def main() -> int:
     ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of the step")
     ap.add_argument("--sweep", action="store_true",
                     help="one line per point of the throughput sweep (drafts x batch, and the long prefill)")
+    ap.add_argument("--profile", action="store_true",
+                    help="for profilers: warmup + steps plain passes of the first index set, no timing, no output")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.sweep:
         return run_sweep(args)
+    if args.profile:
+        return run_profile(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -618,7 +621,6 @@ def main() -> int:
     dbs = [to_device(b) for b in batches]
     algs = [algorithmic_bytes(b) for b in batches]
     batch, db = batches[0], dbs[0]
-    fused = fused_step(batch)
     T = batch.num_actual_tokens
     assert all(b.num_actual_tokens == T for b in batches)
     nsets = len(dbs)
@@ -689,21 +691,15 @@ def main() -> int:
         rec_ms = timed_rotating([rec_fn(d, y) for d, y in zip(dbs, ys)], steps, flush, stream)
         peaks = measured_peaks()
         peak = peaks.get("hbm_gbs")
-        if fused:
-            # the step is the one fused launch: its algorithmic bytes are the whole step's
-            kern_ms, units = step_ms, [a["total"] for a in algs]
-            src = source_hash("gdn_recurrent.cu", "gdn_conv_core.cuh", "gdn_internal.cuh")
-            kname, tkey = "gdn::recurrent_kernel, fused conv (the whole gdn_mixed_batch step)", "recurrent_kernel_fused"
-        else:
-            kern_ms, units = rec_ms, [a["recurrence"] for a in algs]
-            src = source_hash("gdn_recurrent.cu", "gdn_internal.cuh")
-            kname, tkey = "gdn::recurrent_kernel", "recurrent_kernel"
+        kern_ms, units = rec_ms, [a["recurrence"] for a in algs]
+        src = source_hash("gdn_recurrent.cu", "gdn_internal.cuh")
+        kname, tkey = "gdn::recurrent_kernel", "recurrent_kernel"
         roof = {"kernel": kname, "bound": "hbm", "achieved": per_launch_rate(units, kern_ms) / 1e9,
                 "peak": peak or FALLBACK_HBM_GBS, "peak_source": "measured (copy)" if peak else "fallback",
                 "unit": "GB/s", "traffic": recorded_traffic(tkey, args.workload, src),
                 "source_hash": src, "algorithmic_bytes_per_launch": statistics.mean(units),
                 "launch_ms": statistics.median(kern_ms), "launch_ms_mean": statistics.mean(kern_ms),
-                "two_kernel_path_ms": {"conv": statistics.median(conv_ms), "recurrence": statistics.median(rec_ms)}}
+                "conv_launch_ms": statistics.median(conv_ms)}
     roof["frac"] = roof["achieved"] / roof["peak"]
 
     # -------- end to end: pinned host inputs -> device -> gdn_mixed_batch -> host outputs (set 0)
@@ -720,9 +716,7 @@ def main() -> int:
         return 0
 
     chunked = bool(batch.num_prefills and gdn.gdn_prefill_workspace_bytes(db.layer, db.non_spec, batch.num_prefills))
-    # with prefill rows on the chunked path: the recurrence rows (one fused launch, or conv then
-    # recurrence), then the prefill rows' conv (fused layers) and the prep and scan kernels
-    launches_per_step = 4 if chunked else (1 if fused else 2)
+    launches_per_step = 4 if chunked else 2  # conv, recurrence (+ prep and scan of the prefill rows)
     alg_total = statistics.mean(a["total"] for a in algs)
     line = {
         "metric": METRIC, "value": job_throughput(T, world, ms), "unit": UNIT, "n_gpus": world, "steps": steps,

@@ -221,7 +221,6 @@ int gdn_conv_update(const gdn_layer_desc* layer, const gdn_layer_params* params,
   ConvLaunch c = conv_args(layer, params, pools, x, num_global_tokens, d_status);
   c.sub[0] = rows_dev(rows);
   c.y[0] = y;
-  c.count[0] = rows->num_seqs;
   c.units0 = conv_units(rows);
   if (c.units0 > 65535) return GDN_ERR_SHAPE;
   return cuda_rc(launch_conv(c, layer->conv_width, layer->act_dtype, y_dtype, c.units0, (cudaStream_t)stream));
@@ -316,46 +315,27 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
   const int rec_rows = nseq(spec) + (chunked ? num_decodes : nseq(non_spec));
   if (rec_rows > 65535) return GDN_ERR_SHAPE;
 
+  // (1) conv over both subsets in one launch: spec rows first, then the non-spec units.
+  ConvLaunch c = conv_args(layer, params, pools, x, num_actual_tokens, d_status);
+  c.sub[0] = rows_dev(spec);
+  c.y[0] = y_spec;
+  c.units0 = conv_units(spec);
+  c.sub[1] = rows_dev(non_spec);
+  c.y[1] = y_ns;
+  const int units = c.units0 + conv_units(non_spec);
+  if (units > 65535) return GDN_ERR_SHAPE;
+  if ((rc = cuda_rc(launch_conv(c, layer->conv_width, layer->act_dtype, GDN_F32, units, s)))) return rc;
+
+  // (2) token recurrence over the recurrence rows, as a programmatic dependent of the conv.
   RecLaunch r = rec_args(layer, params, pools, a, b, out, num_actual_tokens, d_status);
   r.sub[0] = rows_dev(spec);
+  r.qkv[0] = y_spec;
   r.rows0 = nseq(spec);
   r.sub[1] = rows_dev(non_spec);
+  r.qkv[1] = y_ns;
   r.row_off1 = 0;
-  if (fused_verify_supported(layer)) {
-    // (1) the recurrence rows: conv update and recurrence in one launch (no post-conv workspace)
-    r.conv = conv_args(layer, params, pools, x, num_actual_tokens, d_status);
-    if ((rc = cuda_rc(launch_fused_verify(r, layer->conv_width, layer->act_dtype, rec_rows, s)))) return rc;
-    if (!chunked) return GDN_OK;
-    // (2) the prefill rows: their conv into the workspace, then the chunked prefill
-    ConvLaunch c = conv_args(layer, params, pools, x, num_actual_tokens, d_status);
-    c.sub[1] = rows_dev(non_spec);
-    c.y[1] = y_ns;
-    c.first[1] = num_decodes;
-    c.count[1] = num_prefills;
-    c.units0 = 0;
-    const int units = conv_units(non_spec);
-    if (units > 65535) return GDN_ERR_SHAPE;
-    if ((rc = cuda_rc(launch_conv(c, layer->conv_width, layer->act_dtype, GDN_F32, units, s)))) return rc;
-  } else {
-    // (1) conv over both subsets in one launch: spec rows first, then the non-spec units.
-    ConvLaunch c = conv_args(layer, params, pools, x, num_actual_tokens, d_status);
-    c.sub[0] = rows_dev(spec);
-    c.y[0] = y_spec;
-    c.count[0] = nseq(spec);
-    c.units0 = conv_units(spec);
-    c.sub[1] = rows_dev(non_spec);
-    c.y[1] = y_ns;
-    c.count[1] = nseq(non_spec);
-    const int units = c.units0 + conv_units(non_spec);
-    if (units > 65535) return GDN_ERR_SHAPE;
-    if ((rc = cuda_rc(launch_conv(c, layer->conv_width, layer->act_dtype, GDN_F32, units, s)))) return rc;
-
-    // (2) token recurrence over the recurrence rows, as a programmatic dependent of the conv.
-    r.qkv[0] = y_spec;
-    r.qkv[1] = y_ns;
-    if ((rc = cuda_rc(launch_recurrent(r, layer->act_dtype, GDN_F32, rec_rows, true, s)))) return rc;
-    if (!chunked) return GDN_OK;
-  }
+  if ((rc = cuda_rc(launch_recurrent(r, layer->act_dtype, GDN_F32, rec_rows, true, s)))) return rc;
+  if (!chunked) return GDN_OK;
 
   // (3) chunked prefill of the prefill rows [num_decodes, num_decodes + num_prefills).
   const int chunk_units = prefill_units(non_spec, num_prefills);

@@ -34,10 +34,10 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv_update_kernel(const Conv
   const int unit = s == 0 ? uy : uy - p.units0;
   int n, seg;
   if (R.is_spec) {
-    n = p.first[s] + unit;
+    n = unit;
     seg = 0;
-    if (unit >= p.count[s]) return;
-  } else if (!locate_unit(R, p.first[s], p.count[s], kConvSegNS, unit, n, seg, p.status)) {
+    if (n >= R.num_seqs) return;
+  } else if (!locate_unit(R, 0, R.num_seqs, kConvSegNS, unit, n, seg, p.status)) {
     return;
   }
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;

@@ -14,8 +14,9 @@
 //
 // The thread that reads a slot's history for its VE channels is the only one that ever writes
 // those slot elements, and it writes them only after its reads, so the roll needs no staging
-// buffer and no second pass.  Two kernels use this: the conv kernel (y to global memory) and the
-// fused verify kernel (y to shared memory, one token batch at a time).
+// buffer and no second pass.  The conv kernel runs it with 8 channels per thread (16-byte
+// accesses for bf16); the channel count is a parameter so that a kernel short of registers can
+// take fewer.
 #pragma once
 
 #include "gdn_internal.cuh"

@@ -51,11 +51,3 @@ def test_ragged_prefill_rows_round_up_to_whole_chunks():
     per_chunk = 2 * (5 * c * c * d + 3 * c * d * d + c ** 3 / 6)
     assert bench.prefill_flops(b) == (2 + 1) * 2 * per_chunk   # 65 tokens -> 2 chunks, 64 -> 1; 2 v-heads
 
-
-def test_which_batches_run_as_one_fused_launch():
-    # dk = 128 with (dv / 32) * (Hv / Hk) in {4, 8} and no prefill row on the chunked path
-    assert bench.fused_step(W.spec_verify())
-    assert bench.fused_step(W.non_spec_decode())
-    assert not bench.fused_step(W.mixed())          # prefill rows take the chunked kernels
-    assert not bench.fused_step(W.long_prefill(128))
-    assert not bench.fused_step(W.tiny())           # dk = 16 runs conv then recurrence
