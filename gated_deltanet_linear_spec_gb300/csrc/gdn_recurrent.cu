@@ -184,10 +184,6 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   }
   if (!slot_ok && reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
 
-  // q|k|v may come from the conv grid launched just before (programmatic dependent launch):
-  // everything above touched only the state pool and metadata; wait for that grid here.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
   const QT* __restrict__ qkv = static_cast<const QT*>(p.qkv[s]);
   const ACT* __restrict__ ga = static_cast<const ACT*>(p.a);
   const ACT* __restrict__ gb = static_cast<const ACT*>(p.b);
@@ -195,6 +191,35 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   const int warp = tid / 32, lane = tid % 32;
   const float neg_A = -expf(__ldg(p.A_log + h));
   const float dtb = __ldg(p.dt_bias + h);
+
+  // Gate inputs, global tokens and store slots of a token batch, through lane 0 of each token's
+  // warp (warp w takes tokens w, w+NWARP, ...).  None of them comes from the conv grid.
+  float av[TPW], bv[TPW];
+  int gt_[TPW], ss_[TPW];
+  auto load_gates = [&](int tb0, int nt) {
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+      const int t = warp + u * NWARP;
+      av[u] = bv[u] = 0.f;
+      gt_[u] = -1;
+      ss_[u] = -1;
+      if (t < nt && lane == 0) {
+        const int gt = global_token(R, (int32_t)(bos + tb0 + t), p.num_global, p.status);
+        gt_[u] = gt;
+        if (gt >= 0) {
+          av[u] = to_f32(ga[(int64_t)gt * p.Hv + h]);
+          bv[u] = to_f32(gb[(int64_t)gt * p.Hv + h]);
+        }
+        if (R.is_spec) ss_[u] = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + tb0 + t);
+      }
+    }
+  };
+  // the first batch's go out now, beside the state loads, ahead of the wait for the conv grid
+  load_gates(0, min(TB, L));
+
+  // q|k|v may come from the conv grid launched just before (programmatic dependent launch):
+  // everything above touched only the state pool, the gates and metadata; wait for that grid.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   for (int tb0 = 0; tb0 < L; tb0 += TB) {
     const int nt = min(TB, L - tb0);
@@ -234,24 +259,7 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
         else sV[t][c - 2 * DK] = to_f32(qkv[i * p.C + 2LL * p.Hk * DK + (int64_t)h * p.dv + dv0 + c - 2 * DK]);
       }
     }
-    float av[TPW], bv[TPW];
-    int gt_[TPW], ss_[TPW];
-#pragma unroll
-    for (int u = 0; u < TPW; ++u) {
-      const int t = warp + u * NWARP;
-      av[u] = bv[u] = 0.f;
-      gt_[u] = -1;
-      ss_[u] = -1;
-      if (t < nt && lane == 0) {
-        const int gt = global_token(R, (int32_t)(bos + tb0 + t), p.num_global, p.status);
-        gt_[u] = gt;
-        if (gt >= 0) {
-          av[u] = to_f32(ga[(int64_t)gt * p.Hv + h]);
-          bv[u] = to_f32(gb[(int64_t)gt * p.Hv + h]);
-        }
-        if (R.is_spec) ss_[u] = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + tb0 + t);
-      }
-    }
+    if (tb0) load_gates(tb0, nt);
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // 2b. the arithmetic, in place: L2-normalised q^ (scaled), k^, k^.q^, gates, slots
