@@ -25,8 +25,16 @@
 
 namespace gdn {
 
+#ifndef GDN_CONV_VE
+#define GDN_CONV_VE 4  // channels per thread
+#endif
+#ifndef GDN_CONV_MINB
+#define GDN_CONV_MINB 6  // resident CTAs per SM the register allocation must allow
+#endif
+constexpr int kConvVE = GDN_CONV_VE;
+
 template <typename T, typename YT, int W>
-__global__ void __launch_bounds__(kConvThreads, 4) conv_update_kernel(const ConvLaunch p) {
+__global__ void __launch_bounds__(kConvThreads, GDN_CONV_MINB) conv_update_kernel(const ConvLaunch p) {
   asm volatile("griddepcontrol.launch_dependents;");
   const int uy = blockIdx.y;
   const int s = uy < p.units0 ? 0 : 1;
@@ -40,14 +48,14 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv_update_kernel(const Conv
   } else if (!locate_unit(R, 0, R.num_seqs, kConvSegNS, unit, n, seg, p.status)) {
     return;
   }
-  const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
+  const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * kConvVE;
   if (c0 >= p.C) return;
   const bool reporter = (c0 == 0);
 
   // Loads that do not depend on one another go out together: the row's token range, its
   // acceptance, its own (or column-0) slot, and the thread's weights.
   const ConvRow row = conv_row(R, n);
-  ConvThread<T, W, 8> ct;
+  ConvThread<T, W, kConvVE> ct;
   ct.load_params(p, c0);
 
   if (row.bos < 0 || row.eos < row.bos || row.eos > R.num_tokens) {
@@ -68,13 +76,13 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv_update_kernel(const Conv
   if (!ct.begin(p, R, n, row, seg, t0, reporter)) return;
   YT* __restrict__ y = static_cast<YT*>(p.y[s]);
   ct.tokens(p, R, n, row, t0, t1, reporter,
-            [&](int t, const float(&out)[8]) { store_f32v<YT, 8>(y + (int64_t)(row.bos + t) * p.C + c0, out); });
+            [&](int t, const float(&out)[kConvVE]) { store_f32v<YT, kConvVE>(y + (int64_t)(row.bos + t) * p.C + c0, out); });
   ct.finish(p, R, row, t1 == L);
 }
 
 template <typename T, typename YT>
 static cudaError_t launch_w(const ConvLaunch& p, int width, int units, cudaStream_t s) {
-  const dim3 grid((p.C / 8 + kConvThreads - 1) / kConvThreads, units);
+  const dim3 grid((p.C / kConvVE + kConvThreads - 1) / kConvThreads, units);
   switch (width) {
     case 2: conv_update_kernel<T, YT, 2><<<grid, kConvThreads, 0, s>>>(p); break;
     case 3: conv_update_kernel<T, YT, 3><<<grid, kConvThreads, 0, s>>>(p); break;

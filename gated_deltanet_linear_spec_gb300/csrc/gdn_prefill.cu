@@ -196,6 +196,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const int64_t C = p.C;
   const int qoff = kh * kD, koff = p.Hk * kD + kh * kD, voff = 2 * p.Hk * kD + h * kD;
 
+  // 0. the chunk's v rows start their trip to shared memory at once (cp.async, no registers
+  //    held), into the T / A region, which nothing uses before the first product completes;
+  //    right after it they become the beta v operand rows
+  constexpr uint32_t kVStage = 65536;  // [kCh][kD] QT at sm + kVStage, up to 32 KiB
+  {
+    constexpr int VCH = kD * (int)sizeof(QT) / 16;  // 16-byte chunks per v row
+    const uint32_t dst0 = tc::smem_addr(sm + kVStage);
+    const uint8_t* src0 = reinterpret_cast<const uint8_t*>(qkv + (int64_t)(bos + t0) * C + voff);
+    for (int i = tid; i < nc * VCH; i += kPrepThreads)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + 16 * i),
+                   "l"(src0 + (int64_t)(i / VCH) * C * (int64_t)sizeof(QT) + 16 * (i % VCH))
+                   : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+
   // 1. gates (padded tokens: g = 0, beta = 0), TMEM and barrier
   if (tid < kCh) {
     float g = 0.f, beta = 0.f;
@@ -307,6 +322,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   bool ok = __syncthreads_and(tc::mbar_wait(&bar, 0, p.wait_ns));
   if (ok) {
     tc::fence_after();
+    // 3b. the rows beta_s v_s into the q^ half of the images, which MMA 1 no longer needs (the
+    //     A operand of MMA 3, read MN-major like MMA 2's); the staged v rows are consumed here,
+    //     before the A rows below overwrite their shared memory
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    for (int i = tid; i < kCh * (kD / 4); i += kPrepThreads) {
+      const int t = i / (kD / 4), d0 = 4 * (i % (kD / 4));
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t < nc) {
+        load4(reinterpret_cast<const QT*>(sm + kVStage) + t * kD + d0, x);
+        const float bs = sBeta[t];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] *= bs;
+      }
+      put4_pair(qk_hi, qk_lo, t, d0, 2, x);
+    }
+    __syncthreads();
     // 4. P rows to the record (lane quarters 0, 1: q rows); A rows to shared memory (quarters
     //    2, 3: k rows); warp w reads columns 32 (w / 4) .. +31 of its quarter's rows
     const int quarter = warp & 3, chalf = warp >> 2;
@@ -411,24 +443,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         }
       }
     } else {
-      // 6b. meanwhile, on warps 4-7: the A operands of MMA 2 and 3, both read MN-major (a [s][d]
-      //     tile laid out like a K-major one): the rows beta_s v_s in the q^ half, which MMA 1
-      //     no longer needs, and the k^ rows of the [q^; k^] images scaled in place by
+      // 6b. meanwhile, on warps 4-7: the A operand of MMA 2, read MN-major (a [s][d] tile laid
+      //     out like a K-major one): the k^ rows of the [q^; k^] images scaled in place by
       //     beta_s gamma_s; on the way, the record's K' rows e^{G_c - G_s} k^_s (the same layout).
-      //     The v loads are issued first and stay in flight during the k^ pass.
       const float Gc = sG[kCh - 1], Gcl = sGl[kCh - 1];
-      const int tw0 = (warp - 4) * 16;  // warp 4 + i takes v rows 16i .. 16i+15; lane = 4 dv
-      float v[16][4];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int t = tw0 + u;
-        if (t < nc) {
-          load4(qkv + (int64_t)(bos + t0 + t) * C + voff + 4 * lane, v[u]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[u][e] = 0.f;
-        }
-      }
       for (int i = tid - 128; i < kCh * (kD / 8); i += 128) {
         const int t = i / (kD / 8), d0 = 8 * (i % (kD / 8));
         const uint32_t off = tc::img_off(kCh + t, d0, 2);
@@ -451,15 +469,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         tc::split8(x, nh, nl);
         *reinterpret_cast<uint4*>(qk_hi + off) = nh;
         *reinterpret_cast<uint4*>(qk_lo + off) = nl;
-      }
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int t = tw0 + u;
-        const float bs = sBeta[t];
-        float x[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = bs * v[u][e];
-        put4_pair(qk_hi, qk_lo, t, 4 * lane, 2, x);
       }
       if (tid == 128) *reinterpret_cast<float*>(rec + kMeta) = expf(Gc);
     }
@@ -516,6 +525,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     if (tid == 0) set_status(p.status, GDN_STATUS_WAIT_TIMEOUT);
     tc::mbar_wait(&bar, 0, p.wait_ns);  // bounded: let any issued MMA drain before TMEM is released
     tc::mbar_wait(&bar, 1, p.wait_ns);
+    asm volatile("cp.async.wait_all;" ::: "memory");  // and the staged v rows (if MMA 1 never came)
   }
   tc::fence_before();
   __syncthreads();

@@ -193,29 +193,45 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
   const float dtb = __ldg(p.dt_bias + h);
 
   // Gate inputs, global tokens and store slots of a token batch, through lane 0 of each token's
-  // warp (warp w takes tokens w, w+NWARP, ...).  None of them comes from the conv grid.
+  // warp (warp w takes tokens w, w+NWARP, ...).  None of them comes from the conv grid: the
+  // first batch's token indices and store slots are loaded before the wait for that grid (not
+  // used until after it, so nothing stalls on them there), the gate inputs they address right
+  // after the q|k|v copies are issued.
   float av[TPW], bv[TPW];
   int gt_[TPW], ss_[TPW];
-  auto load_gates = [&](int tb0, int nt) {
+  auto load_tokens = [&](int tb0, int nt) {
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+      const int t = warp + u * NWARP;
+      gt_[u] = -1;
+      ss_[u] = -1;
+      if (t < nt && lane == 0) {
+        const int32_t i = bos + tb0 + t;
+        gt_[u] = R.tok ? __ldg(R.tok + i) : i;
+        if (R.is_spec) ss_[u] = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + tb0 + t);
+      }
+    }
+  };
+  auto load_gates = [&](int nt) {
 #pragma unroll
     for (int u = 0; u < TPW; ++u) {
       const int t = warp + u * NWARP;
       av[u] = bv[u] = 0.f;
-      gt_[u] = -1;
-      ss_[u] = -1;
       if (t < nt && lane == 0) {
-        const int gt = global_token(R, (int32_t)(bos + tb0 + t), p.num_global, p.status);
+        int gt = gt_[u];
+        if (gt < 0 || gt >= p.num_global) {
+          set_status(p.status, GDN_STATUS_TOKEN_RANGE);
+          gt = -1;
+        }
         gt_[u] = gt;
         if (gt >= 0) {
           av[u] = to_f32(ga[(int64_t)gt * p.Hv + h]);
           bv[u] = to_f32(gb[(int64_t)gt * p.Hv + h]);
         }
-        if (R.is_spec) ss_[u] = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + tb0 + t);
       }
     }
   };
-  // the first batch's go out now, beside the state loads, ahead of the wait for the conv grid
-  load_gates(0, min(TB, L));
+  load_tokens(0, min(TB, L));
 
   // q|k|v may come from the conv grid launched just before (programmatic dependent launch):
   // everything above touched only the state pool, the gates and metadata; wait for that grid.
@@ -259,7 +275,8 @@ __global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const
         else sV[t][c - 2 * DK] = to_f32(qkv[i * p.C + 2LL * p.Hk * DK + (int64_t)h * p.dv + dv0 + c - 2 * DK]);
       }
     }
-    if (tb0) load_gates(tb0, nt);
+    if (tb0) load_tokens(tb0, nt);
+    load_gates(nt);
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // 2b. the arithmetic, in place: L2-normalised q^ (scaled), k^, k^.q^, gates, slots
