@@ -26,10 +26,10 @@
 namespace gdn {
 
 #ifndef GDN_CONV_VE
-#define GDN_CONV_VE 4  // channels per thread
+#define GDN_CONV_VE 8  // channels per thread
 #endif
 #ifndef GDN_CONV_MINB
-#define GDN_CONV_MINB 6  // resident CTAs per SM the register allocation must allow
+#define GDN_CONV_MINB 4  // resident CTAs per SM the register allocation must allow
 #endif
 constexpr int kConvVE = GDN_CONV_VE;
 

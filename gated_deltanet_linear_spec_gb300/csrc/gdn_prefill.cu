@@ -196,10 +196,24 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const int64_t C = p.C;
   const int qoff = kh * kD, koff = p.Hk * kD + kh * kD, voff = 2 * p.Hk * kD + h * kD;
 
-  // 0. the chunk's v rows start their trip to shared memory at once (cp.async, no registers
-  //    held), into the T / A region, which nothing uses before the first product completes;
-  //    right after it they become the beta v operand rows
-  constexpr uint32_t kVStage = 65536;  // [kCh][kD] QT at sm + kVStage, up to 32 KiB
+  // 0. every row the chunk reads starts its trip to shared memory at once (cp.async, no
+  //    registers held): the q and k rows into the image region they are turned into (one
+  //    commit group), the v rows into the T / A region, which nothing uses before the first
+  //    product completes; right after it they become the beta v operand rows (a second group)
+  constexpr uint32_t kQStage = 0, kKStage = 32768;  // [kCh][kD] QT each, up to 32 KiB
+  constexpr uint32_t kVStage = 65536;               // [kCh][kD] QT at sm + kVStage, up to 32 KiB
+  {
+    constexpr int RCH = kD * (int)sizeof(QT) / 16;  // 16-byte chunks per row
+    const uint32_t dq = tc::smem_addr(sm + kQStage), dkk = tc::smem_addr(sm + kKStage);
+    const uint8_t* srcq = reinterpret_cast<const uint8_t*>(qkv + (int64_t)(bos + t0) * C + qoff);
+    const uint8_t* srck = reinterpret_cast<const uint8_t*>(qkv + (int64_t)(bos + t0) * C + koff);
+    for (int i = tid; i < nc * RCH; i += kPrepThreads) {
+      const int64_t go = (int64_t)(i / RCH) * C * (int64_t)sizeof(QT) + 16 * (i % RCH);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dq + 16 * i), "l"(srcq + go) : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dkk + 16 * i), "l"(srck + go) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   {
     constexpr int VCH = kD * (int)sizeof(QT) / 16;  // 16-byte chunks per v row
     const uint32_t dst0 = tc::smem_addr(sm + kVStage);
@@ -257,25 +271,27 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   __syncthreads();
 
   // 2. q^ (scaled) and k^ rows of the [q^; k^] images, and the gamma q^ record rows; warp w
-  //    takes tokens 8w .. 8w+7, their loads in flight together
+  //    takes tokens 8w .. 8w+7: their raw rows from shared memory into registers, then (once
+  //    every warp holds its rows) the images over the raw rows
   {
-    constexpr int i0 = 0;
+    asm volatile("cp.async.wait_group 1;" ::: "memory");  // the q and k rows (v may still be in flight)
+    __syncthreads();
     float q[8][4], k[8][4];
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
-      const int t = warp * 8 + i0 + b;
+      const int t = warp * 8 + b;
       if (t < nc) {
-        const QT* row = qkv + (int64_t)(bos + t0 + t) * C;
-        load4(row + qoff + 4 * lane, q[b]);
-        load4(row + koff + 4 * lane, k[b]);
+        load4(reinterpret_cast<const QT*>(sm + kQStage) + t * kD + 4 * lane, q[b]);
+        load4(reinterpret_cast<const QT*>(sm + kKStage) + t * kD + 4 * lane, k[b]);
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) q[b][e] = k[b][e] = 0.f;
       }
     }
+    __syncthreads();
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
-      const int t = warp * 8 + i0 + b;
+      const int t = warp * 8 + b;
       float sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
