@@ -539,10 +539,6 @@ def run_sweep(args) -> int:
                                          steps, flush, stream))
             roof = {"kernel": "gdn_chunk_prefill", "bound": "tensor", "unit": "TFLOP/s", "peak": bf16,
                     "achieved": prefill_flops(batch) / (k_ms * 1e-3) / 1e12, "launch_ms": k_ms}
-        elif gdn.gdn_testing_verify_path_of(db.layer, db.non_spec, db.num_prefills, db.spec) == 2:
-            roof = {"kernel": "gdn::recurrent_kernel with the fused conv (the whole step)", "bound": "hbm",
-                    "unit": "GB/s", "peak": hbm, "achieved": alg["total"] / (ms * 1e-3) / 1e9, "launch_ms": ms,
-                    "algorithmic_bytes_per_launch": alg["total"]}
         else:
             k_ms = statistics.median(timed(lambda: gdn.gdn_recurrent_step(db.layer, db.params, db.pools, y, db.a, db.b,
                                                                         rows, db.out, db.status),
@@ -578,16 +574,10 @@ def main() -> int:
     ap.add_argument("--graph", action="store_true", help="time replays of a CUDA graph of the step")
     ap.add_argument("--sweep", action="store_true",
                     help="one line per point of the throughput sweep (drafts x batch, and the long prefill)")
-    ap.add_argument("--verify-path", default="auto", choices=["auto", "two", "fused"],
-                    help="recurrence rows through the kernels chosen by size (auto), the conv kernel then the "
-                         "recurrence (two), or the fused kernel where the batch allows it (fused)")
     ap.add_argument("--profile", action="store_true",
                     help="for profilers: warmup + steps plain passes of the first index set, no timing, no output")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    if args.verify_path != "auto":
-        import gated_deltanet_linear_spec_gb300 as gdn
-        gdn.gdn_testing_set_verify_path({"two": 1, "fused": 2}[args.verify_path])
     if args.sweep:
         return run_sweep(args)
     if args.profile:
@@ -701,15 +691,9 @@ def main() -> int:
         rec_ms = timed_rotating([rec_fn(d, y) for d, y in zip(dbs, ys)], steps, flush, stream)
         peaks = measured_peaks()
         peak = peaks.get("hbm_gbs")
-        if gdn.gdn_testing_verify_path_of(db.layer, db.non_spec, db.num_prefills, db.spec) == 2:
-            # the step is one launch of the fused kernel: its algorithmic bytes are the step's
-            kern_ms, units = step_ms, [a["total"] for a in algs]
-            src = source_hash("gdn_recurrent.cu", "gdn_conv_core.cuh", "gdn_internal.cuh")
-            kname, tkey = "gdn::recurrent_kernel with the fused conv (the whole step)", "recurrent_kernel_fused"
-        else:
-            kern_ms, units = rec_ms, [a["recurrence"] for a in algs]
-            src = source_hash("gdn_recurrent.cu", "gdn_internal.cuh")
-            kname, tkey = "gdn::recurrent_kernel", "recurrent_kernel"
+        kern_ms, units = rec_ms, [a["recurrence"] for a in algs]
+        src = source_hash("gdn_recurrent.cu", "gdn_internal.cuh")
+        kname, tkey = "gdn::recurrent_kernel", "recurrent_kernel"
         roof = {"kernel": kname, "bound": "hbm", "achieved": per_launch_rate(units, kern_ms) / 1e9,
                 "peak": peak or FALLBACK_HBM_GBS, "peak_source": "measured (copy)" if peak else "fallback",
                 "unit": "GB/s", "traffic": recorded_traffic(tkey, args.workload, src),
@@ -732,9 +716,7 @@ def main() -> int:
         return 0
 
     chunked = bool(batch.num_prefills and gdn.gdn_prefill_workspace_bytes(db.layer, db.non_spec, batch.num_prefills))
-    # conv, recurrence (+ prep and scan of the prefill rows); one launch on the fused path
-    one = gdn.gdn_testing_verify_path_of(db.layer, db.non_spec, db.num_prefills, db.spec) == 2
-    launches_per_step = 4 if chunked else (1 if one else 2)
+    launches_per_step = 4 if chunked else 2  # conv, recurrence (+ prep and scan of the prefill rows)
     alg_total = statistics.mean(a["total"] for a in algs)
     line = {
         "metric": METRIC, "value": job_throughput(T, world, ms), "unit": UNIT, "n_gpus": world, "steps": steps,

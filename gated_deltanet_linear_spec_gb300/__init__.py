@@ -64,7 +64,7 @@ class _Rows(ctypes.Structure):
 EXPORTS = ("gdn_workspace_bytes", "gdn_prefill_workspace_bytes", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
            "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "gdn_status_string")
 # include/gdn_testing.h: hooks that let tests drive the kernels' failure paths
-TESTING_EXPORTS = ("gdn_testing_set_prefill_faults", "gdn_testing_set_verify_path", "gdn_testing_verify_path_of", "gdn_testing_verify_path_of")
+TESTING_EXPORTS = ("gdn_testing_set_prefill_faults",)
 STATIC_WORKSPACE_BYTES = 16 << 20
 
 _lib = None
@@ -103,10 +103,6 @@ def library() -> ctypes.CDLL:
                                                              I32, P(_Rows), I32, I32, P(_Rows), VP, VP, VP]
             lib.gdn_testing_set_prefill_faults.restype = ctypes.c_int
             lib.gdn_testing_set_prefill_faults.argtypes = [ctypes.c_uint64, I32]
-            lib.gdn_testing_set_verify_path.restype = ctypes.c_int
-            lib.gdn_testing_set_verify_path.argtypes = [I32]
-            lib.gdn_testing_verify_path_of.restype = ctypes.c_int
-            lib.gdn_testing_verify_path_of.argtypes = [P(_LayerDesc), P(_Rows), I32, P(_Rows)]
             _lib = lib
     return _lib
 
@@ -316,25 +312,8 @@ def gdn_testing_set_prefill_faults(wait_ns: int = 0, drop_copy_chunk: int = -1) 
     _check(library().gdn_testing_set_prefill_faults(int(wait_ns), int(drop_copy_chunk)))
 
 
-def gdn_testing_set_verify_path(path: int = 0) -> None:
-    """Test hook (include/gdn_testing.h): 0 = the verify kernels chosen by size, 1 = the conv
-    kernel then the recurrence, 2 = the fused kernel whenever the batch allows it."""
-    _check(library().gdn_testing_set_verify_path(int(path)))
-
-
-def gdn_testing_verify_path_of(layer: Layer, non_spec: Optional[Rows], num_prefills: int,
-                               spec: Optional[Rows]) -> int:
-    """Test hook (include/gdn_testing.h): 1 if gdn_mixed_batch would run this batch's recurrence
-    rows as the conv kernel then the recurrence, 2 if through the fused kernel."""
-    rc = library().gdn_testing_verify_path_of(ctypes.byref(layer.c()), _rows_ref(non_spec), int(num_prefills),
-                                              _rows_ref(spec))
-    if rc < 0:
-        _check(rc)
-    return rc
-
-
 __all__ = ["Layer", "Params", "Pools", "Rows", "GdnError", "library", "LIB_PATH", "EXPORTS",
            "gdn_workspace_bytes", "gdn_prefill_workspace_bytes", "mixed_batch_workspace_bytes", "STATUS_WAIT_TIMEOUT", "gdn_conv_update", "gdn_recurrent_step", "gdn_chunk_prefill",
            "gdn_mixed_batch", "gdn_mixed_batch_static_workspace", "STATIC_WORKSPACE_BYTES",
-           "TESTING_EXPORTS", "gdn_testing_set_prefill_faults", "gdn_testing_set_verify_path", "gdn_testing_verify_path_of", "GDN_F32", "GDN_BF16", "STATUS_SLOT_RANGE", "STATUS_NUM_ACCEPTED",
+           "TESTING_EXPORTS", "gdn_testing_set_prefill_faults", "GDN_F32", "GDN_BF16", "STATUS_SLOT_RANGE", "STATUS_NUM_ACCEPTED",
            "STATUS_TOKEN_RANGE", "STATUS_ROW_RANGE"]

@@ -11,33 +11,11 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <atomic>
-
 #include "gdn_internal.cuh"
-#include "gdn_testing.h"
 
 using namespace gdn;
 
 namespace {
-
-// Test hook (gdn_testing.h): 0 = choose the verify kernels by size, 1 = always the conv kernel
-// then the recurrence, 2 = the fused kernel whenever the batch allows it.
-std::atomic<int32_t> g_verify_path{0};
-
-// Streaming multiprocessors of the current device (looked up once per device).
-int sm_count() {
-  static std::atomic<int> cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64) {
-    int n = cache[dev].load(std::memory_order_relaxed);
-    if (n > 0) return n;
-  }
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
-  return n;
-}
 
 constexpr int kMaxSpecCols = 64;  // a spec row is one conv work unit of kConvSeg tokens
 
@@ -143,17 +121,6 @@ float resolve_scale(const gdn_layer_desc* d) {
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
-
-// Whether gdn_mixed_batch runs its recurrence rows through the fused verify kernel: the layer
-// allows it, no prefill row takes the chunked path, and (unless a test forces a path) the fused
-// grid fits in one wave of the current device.
-bool take_fused(const gdn_layer_desc* layer, bool chunked, int rec_rows) {
-  if (chunked || rec_rows <= 0 || !fused_verify_supported(layer)) return false;
-  const int mode = g_verify_path.load(std::memory_order_relaxed);
-  if (mode != 0) return mode == 2;
-  const int64_t ctas = (int64_t)rec_rows * layer->num_v_heads * (layer->head_v_dim / 32);
-  return ctas <= (int64_t)sm_count() * fused_verify_ctas_per_sm();
-}
 
 ConvLaunch conv_args(const gdn_layer_desc* d, const gdn_layer_params* prm, const gdn_pools* pools,
                      const void* x, int32_t num_global, uint32_t* status) {
@@ -348,18 +315,6 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
   const int rec_rows = nseq(spec) + (chunked ? num_decodes : nseq(non_spec));
   if (rec_rows > 65535) return GDN_ERR_SHAPE;
 
-  // Small batches whose recurrence rows are all the batch holds: one fused launch (conv and
-  // recurrence, one dependent chain per CTA) when its grid fits in one wave of the GPU.
-  if (take_fused(layer, chunked, rec_rows)) {
-    RecLaunch r = rec_args(layer, params, pools, a, b, out, num_actual_tokens, d_status);
-    r.sub[0] = rows_dev(spec);
-    r.rows0 = nseq(spec);
-    r.sub[1] = rows_dev(non_spec);
-    r.row_off1 = 0;
-    r.conv = conv_args(layer, params, pools, x, num_actual_tokens, d_status);
-    return cuda_rc(launch_fused_verify(r, layer->conv_width, layer->act_dtype, rec_rows, s));
-  }
-
   // (1) conv over both subsets in one launch: spec rows first, then the non-spec units.
   ConvLaunch c = conv_args(layer, params, pools, x, num_actual_tokens, d_status);
   c.sub[0] = rows_dev(spec);
@@ -387,20 +342,6 @@ int gdn_mixed_batch(const gdn_layer_desc* layer, const gdn_layer_params* params,
   PrefillLaunch p = prefill_args(layer, params, pools, y_ns, a, b, out, num_actual_tokens, non_spec, num_decodes,
                                  num_prefills, ws_prefill, d_status);
   return cuda_rc(launch_prefill(p, GDN_F32, chunk_units, s));
-}
-
-int gdn_testing_verify_path_of(const gdn_layer_desc* layer, const gdn_rows* non_spec, int32_t num_prefills,
-                               const gdn_rows* spec) {
-  if (check_layer(layer) || check_rows(layer, non_spec) || check_rows(layer, spec)) return GDN_ERR_SHAPE;
-  const bool chunked = num_prefills > 0 && prefill_tc_supported(layer);
-  const int rec_rows = nseq(spec) + (chunked ? nseq(non_spec) - num_prefills : nseq(non_spec));
-  return take_fused(layer, chunked, rec_rows) ? 2 : 1;
-}
-
-int gdn_testing_set_verify_path(int32_t path) {
-  if (path < 0 || path > 2) return GDN_ERR_SHAPE;
-  g_verify_path.store(path, std::memory_order_relaxed);
-  return GDN_OK;
 }
 
 }  // extern "C"

@@ -248,7 +248,6 @@ struct RecLaunch {
   int32_t rows0;     // grid.z rows of subset 0
   int32_t row_off1;  // first row of subset 1 handled by this launch
   uint32_t* status;
-  ConvLaunch conv;   // the fused verify kernel's conv update (unused by the plain recurrence)
 };
 
 // Chunked prefill (tensor-core path): chunk length and the per (chunk, v-head) record size.
@@ -286,12 +285,6 @@ cudaError_t launch_conv(const ConvLaunch& p, int width, gdn_dtype act, gdn_dtype
 // pdl: launch as a programmatic dependent of the kernel just before it on the stream.
 cudaError_t launch_recurrent(const RecLaunch& p, gdn_dtype act, gdn_dtype qkv_dtype, int rows_total, bool pdl,
                              cudaStream_t s);
-// The fused verify kernel (conv update and recurrence in one launch, a thread-block cluster per
-// (row, k-head)) covers layers with dk = 128, dv a multiple of 32 and (dv / 32) * (Hv / Hk) in
-// {4, 8}; fused_verify_ctas_per_sm() is its resident CTAs per SM.
-bool fused_verify_supported(const gdn_layer_desc* d);
-int fused_verify_ctas_per_sm();
-cudaError_t launch_fused_verify(const RecLaunch& p, int width, gdn_dtype act, int rows_total, cudaStream_t s);
 // The tensor-core chunked prefill handles dk = dv = 128 with bf16 activations.
 bool prefill_tc_supported(const gdn_layer_desc* d);
 cudaError_t launch_prefill(const PrefillLaunch& p, gdn_dtype qkv_dtype, int units_upper, cudaStream_t s);

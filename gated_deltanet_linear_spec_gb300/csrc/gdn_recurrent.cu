@@ -30,31 +30,9 @@
 // kernel follows as a programmatic dependent launch.  Each thread stores exactly the elements
 // it loaded, after loading them, so the load slot may also be a store slot (t = num_accepted-1)
 // without a hazard.
-#include "gdn_conv_core.cuh"
+#include "gdn_internal.cuh"
 
 namespace gdn {
-
-// ---- thread-block clusters (the fused verify kernel) -----------------------------------------
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster arrives, then waits for all arrivals of the phase;
-// release / acquire order the shared-memory writes before the arrival against reads after it.
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-// 16 bytes of CTA `rank`'s shared memory at the address `local` has in this CTA's.
-__device__ __forceinline__ float4 ld_cluster_f4(const void* local, uint32_t rank) {
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(ra)
-               : "memory");
-  return v;
-}
 
 #ifndef GDN_REC_LD_HINT
 #define GDN_REC_LD_HINT 0  // 0: L1 no-allocate; 1: also ask L2 for 256-byte prefetch
@@ -99,22 +77,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 #ifndef GDN_REC_MINB
 #define GDN_REC_MINB 8  // resident CTAs per SM the register allocation must allow
 #endif
-#ifndef GDN_FUSED_MINB
-#define GDN_FUSED_MINB 7  // the same for the fused verify kernel (its conv threads need more)
-#endif
 
-// FW > 0 selects the fused verify kernel: the conv update of width FW runs inside the launch.
-// The CTAs of one (row, k-head) -- every dv tile of its Hv/Hk v-heads, NC in all -- form a
-// thread-block cluster.  Each CTA convolves a disjoint slice of the conv channels: 2*DK/NC of the
-// k-head's q|k channels and its own DVT*TPC v channels, two channels per thread, so it is the only
-// reader and writer of those conv-slot elements (the ring is rolled with no staging and no second
-// pass).  The q|k outputs are exchanged through distributed shared memory, one token batch at a
-// time, between two cluster barriers.  A CTA's path is then one dependent chain (metadata, history
-// and x, conv, exchange, recurrence) instead of the conv grid's chain followed by its own, which
-// pays off when the whole grid is one wave; over many waves the cluster barriers hold every CTA
-// of a cluster to the slowest one and the plain kernel behind the conv grid is faster.
-template <typename ACT, typename QT, int DK, int DVT, int LPR, int TB, int TPC, int FW = 0, int NC = 1>
-__global__ void __launch_bounds__(DVT* LPR, FW > 0 ? GDN_FUSED_MINB : GDN_REC_MINB) recurrent_kernel(const RecLaunch p) {
+template <typename ACT, typename QT, int DK, int DVT, int LPR, int TB, int TPC>
+__global__ void __launch_bounds__(DVT* LPR, GDN_REC_MINB) recurrent_kernel(const RecLaunch p) {
   static_assert(TPC == 1 || TPC == 2 || TPC == 4, "1, 2 or 4 tiles per CTA");
   constexpr int NT = DVT * LPR;
   constexpr int EPT = DK / LPR;  // fp32 state elements per thread
@@ -133,13 +98,6 @@ __global__ void __launch_bounds__(DVT* LPR, FW > 0 ? GDN_FUSED_MINB : GDN_REC_MI
   __shared__ __align__(16) float4 sSt[TPC > 1 ? (TPC - 1) * NV * NT : 1];
   __shared__ float sEg[TB], sBeta[TB], sKQ[TB];
   __shared__ int32_t sStore[TB], sGt[TB];
-  // fused: this CTA's conv outputs of a token batch, its q|k slice then its v channels
-  constexpr int QKC = FW > 0 ? 2 * DK / NC : 0;  // q|k channels convolved here
-  constexpr int YW = FW > 0 ? QKC + DVT * TPC : 4;
-  constexpr int CVE = 2;                          // channels per conv thread
-  constexpr int NCONV = FW > 0 ? YW / CVE : 0;    // conv threads
-  static_assert(FW == 0 || (NC * QKC == 2 * DK && QKC % 4 == 0 && NCONV <= DVT * LPR), "fused tile");
-  __shared__ __align__(16) float sY[FW > 0 ? TB : 1][YW];
 
   const int tid = threadIdx.x;
   const int rr = tid / LPR;  // state row within the tile
@@ -277,28 +235,7 @@ __global__ void __launch_bounds__(DVT* LPR, FW > 0 ? GDN_FUSED_MINB : GDN_REC_MI
 
   // q|k|v may come from the conv grid launched just before (programmatic dependent launch):
   // everything above touched only the state pool, the gates and metadata; wait for that grid.
-  if constexpr (FW == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // fused: the conv threads take their channels, weights and history (the state loads above
-  // stay in flight)
-  [[maybe_unused]] ConvThread<ACT, (FW > 0 ? FW : 2), CVE> ct;
-  [[maybe_unused]] ConvRow crow;
-  [[maybe_unused]] const bool conv_thr = FW > 0 && tid < NCONV;
-  if constexpr (FW > 0) {
-    if (conv_thr) {
-      const int j = tid * CVE;  // column in sY
-      int c;
-      if (j < QKC) {
-        const int qi = (int)cluster_ctarank() * QKC + j;  // within q_kh (DK) | k_kh (DK)
-        c = qi < DK ? kh * DK + qi : p.Hk * DK + kh * DK + (qi - DK);
-      } else {
-        c = 2 * p.Hk * DK + h * p.dv + dv0 + (j - QKC);
-      }
-      crow = conv_row(R, n);
-      ct.load_params(p.conv, c);
-      ct.begin(p.conv, R, n, crow, 0, 0, reporter);  // rows with a bad num_accepted were skipped above
-    }
-  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   for (int tb0 = 0; tb0 < L; tb0 += TB) {
     const int nt = min(TB, L - tb0);
@@ -308,12 +245,7 @@ __global__ void __launch_bounds__(DVT* LPR, FW > 0 ? GDN_FUSED_MINB : GDN_REC_MI
     //     round trip: raw q and k rows and this tile's v slice land in shared memory through
     //     cp.async (no registers held), the gate inputs and store slots through lane 0 of each
     //     token's warp.  Warp w prepares tokens w, w+NWARP, ...
-    //     Fused: after the gate loads are out, the conv threads compute this batch's outputs of
-    //     their channels into sY (and roll the conv slot as they go); the q|k rows are then
-    //     gathered from the cluster.
-    if constexpr (FW > 0) {
-      if (tb0) cluster_wait();  // every CTA of the cluster has read the previous batch's sY
-    } else if constexpr (sizeof(QT) == 4 && DK % 4 == 0 && (DVT * TPC) % 4 == 0) {
+    if constexpr (sizeof(QT) == 4 && DK % 4 == 0 && (DVT * TPC) % 4 == 0) {
       constexpr int QC = DK / 4, VC = DVT * TPC / 4;  // 16-byte chunks per q/k row and per v slice
       for (int idx = tid; idx < nt * (2 * QC + VC); idx += NT) {
         const int t = idx / (2 * QC + VC), c = idx % (2 * QC + VC);
@@ -345,31 +277,6 @@ __global__ void __launch_bounds__(DVT* LPR, FW > 0 ? GDN_FUSED_MINB : GDN_REC_MI
     }
     if (tb0) load_tokens(tb0, nt);
     load_gates(nt);
-    if constexpr (FW > 0) {
-      if (conv_thr) {
-        ct.tokens(p.conv, R, n, crow, tb0, tb0 + nt, reporter, [&](int t, const float(&y)[CVE]) {
-          *reinterpret_cast<float2*>(&sY[t - tb0][tid * CVE]) = make_float2(y[0], y[1]);
-        });
-        if (tb0 + nt == L) ct.finish(p.conv, R, crow, true);
-      }
-      // the batch's conv outputs of every CTA of the cluster are complete and visible; gather
-      // this k-head's q|k rows (owner rank = channel / QKC) and this CTA's v slice
-      cluster_arrive();
-      cluster_wait();
-      constexpr int QK4 = 2 * DK / 4, V4 = DVT * TPC / 4;
-      for (int idx = tid; idx < nt * (QK4 + V4); idx += NT) {
-        const int t = idx / (QK4 + V4), c = idx % (QK4 + V4);
-        if (c < QK4) {
-          const int qi = 4 * c;
-          const float4 v = ld_cluster_f4(&sY[t][qi % QKC], (uint32_t)(qi / QKC));
-          *reinterpret_cast<float4*>(qi < DK ? &sQ[t][qi] : &sK[t][qi - DK]) = v;
-        } else {
-          const int vi = 4 * (c - QK4);
-          *reinterpret_cast<float4*>(&sV[t][vi]) = *reinterpret_cast<const float4*>(&sY[t][QKC + vi]);
-        }
-      }
-      cluster_arrive();  // this CTA is done reading the cluster's sY (waited for before reuse)
-    }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // 2b. the arithmetic, in place: L2-normalised q^ (scaled), k^, k^.q^, gates, slots
@@ -495,8 +402,6 @@ __global__ void __launch_bounds__(DVT* LPR, FW > 0 ? GDN_FUSED_MINB : GDN_REC_MI
       }
     }
   }
-  // fused: no CTA leaves (and frees its shared memory) while a peer may still read its sY
-  if constexpr (FW > 0) cluster_wait();
 }
 
 #ifndef GDN_REC_TPC
@@ -539,65 +444,6 @@ static cudaError_t launch_dv(const RecLaunch& p, int rows, bool pdl, cudaStream_
   if (GDN_REC_TPC >= 2 && p.dv % (2 * GDN_REC_DVT) == 0) return launch_tile<ACT, QT, DK, GDN_REC_DVT, 2>(p, rows, pdl, s);
   if (p.dv % GDN_REC_DVT == 0) return launch_tile<ACT, QT, DK, GDN_REC_DVT, 1>(p, rows, pdl, s);
   return launch_tile<ACT, QT, DK, 16, 1>(p, rows, pdl, s);
-}
-
-// The fused verify kernel: dk = 128, two tiles of 16 state rows per CTA (dv / 32 CTAs per
-// v-head), a cluster of NC = (dv / 32) * (Hv / Hk) CTAs per (row, k-head).
-template <typename ACT, int FW, int NC>
-static cudaError_t launch_fused_nc(const RecLaunch& p, int rows, cudaStream_t s) {
-  constexpr int DK = 128, DVT = 16, TPC = 2, LPR = GDN_REC_LPR, TB = 8;
-  auto kern = recurrent_kernel<ACT, float, DK, DVT, LPR, TB, TPC, FW, NC>;
-  const int tiles = p.dv / (DVT * TPC);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles, p.Hv, rows);
-  cfg.blockDim = dim3(DVT * LPR);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = tiles;
-  attr[0].val.clusterDim.y = NC / tiles;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
-template <typename ACT, int FW>
-static cudaError_t launch_fused_w(const RecLaunch& p, int rows, cudaStream_t s) {
-  const int nc = (p.dv / 32) * (p.Hv / p.Hk);
-  if (nc == 8) return launch_fused_nc<ACT, FW, 8>(p, rows, s);
-  if (nc == 4) return launch_fused_nc<ACT, FW, 4>(p, rows, s);
-  return cudaErrorInvalidValue;
-}
-
-bool fused_verify_supported(const gdn_layer_desc* d) {
-  if (d->head_k_dim != 128 || d->head_v_dim % 32 != 0) return false;
-  const int nc = (d->head_v_dim / 32) * (d->num_v_heads / d->num_k_heads);
-  return nc == 4 || nc == 8;
-}
-
-int fused_verify_ctas_per_sm() { return GDN_FUSED_MINB; }
-
-cudaError_t launch_fused_verify(const RecLaunch& p, int width, gdn_dtype act, int rows_total, cudaStream_t s) {
-  if (rows_total <= 0) return cudaSuccess;
-  cudaError_t e;
-  if (act == GDN_BF16) {
-    switch (width) {
-      case 2: e = launch_fused_w<__nv_bfloat16, 2>(p, rows_total, s); break;
-      case 3: e = launch_fused_w<__nv_bfloat16, 3>(p, rows_total, s); break;
-      case 4: e = launch_fused_w<__nv_bfloat16, 4>(p, rows_total, s); break;
-      default: return cudaErrorInvalidValue;
-    }
-  } else {
-    switch (width) {
-      case 2: e = launch_fused_w<float, 2>(p, rows_total, s); break;
-      case 3: e = launch_fused_w<float, 3>(p, rows_total, s); break;
-      case 4: e = launch_fused_w<float, 4>(p, rows_total, s); break;
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename ACT, typename QT>

@@ -14,8 +14,6 @@
 
 #include <stdint.h>
 
-#include "gdn.h"
-
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -32,29 +30,6 @@ extern "C" {
  * returns 0 (GDN_OK).  Reset with gdn_testing_set_prefill_faults(0, -1).
  */
 int gdn_testing_set_prefill_faults(uint64_t wait_ns, int32_t drop_copy_chunk);
-
-/*
- * Which kernels gdn_mixed_batch runs for the token-recurrence rows (spec and decode rows, and
- * every non-spec row when no prefill row takes the chunked path), for every later call in this
- * process:
- *   0  by size (the default): when the layer allows it (dk = 128, dv a multiple of 32,
- *      (dv / 32) * (Hv / Hk) in {4, 8}), the batch has no chunked prefill rows and the fused
- *      kernel's grid fits in one wave of the GPU, the fused kernel (conv update and recurrence
- *      in one launch); otherwise the conv kernel, then the recurrence;
- *   1  always the conv kernel, then the recurrence;
- *   2  the fused kernel whenever the layer and batch allow it, whatever the grid size.
- * Both give the same results bit for bit; the setting only exists so that tests can run each
- * on any batch.  Returns 0, or GDN_ERR_SHAPE (-3) for another value.
- */
-int gdn_testing_set_verify_path(int32_t path);
-
-/*
- * The path gdn_mixed_batch would take for the token-recurrence rows of this batch on the current
- * device under the current setting: 1 (conv kernel, then recurrence) or 2 (fused kernel);
- * GDN_ERR_SHAPE (-3) for invalid descriptors.  Host only: reads no device memory.
- */
-int gdn_testing_verify_path_of(const gdn_layer_desc* layer, const gdn_rows* non_spec, int32_t num_prefills,
-                               const gdn_rows* spec);
 
 #ifdef __cplusplus
 }
