@@ -59,53 +59,6 @@ __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-// 8 consecutive elements as raw 16-byte vectors (1 for bf16, 2 for fp32): bit-exact copies.
-template <typename T>
-struct Raw8 {
-  static constexpr int N = (int)sizeof(T) / 2;  // uint4 per 8 elements
-  uint4 v[N];
-};
-
-template <typename T>
-__device__ __forceinline__ Raw8<T> load_raw8(const T* p) {
-  Raw8<T> r;
-  const uint4* q = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < Raw8<T>::N; ++i) r.v[i] = __ldg(q + i);
-  return r;
-}
-
-template <typename T>
-__device__ __forceinline__ Raw8<T> zero_raw8() {
-  Raw8<T> r;
-#pragma unroll
-  for (int i = 0; i < Raw8<T>::N; ++i) r.v[i] = make_uint4(0u, 0u, 0u, 0u);
-  return r;
-}
-
-template <typename T>
-__device__ __forceinline__ void store_raw8(T* p, const Raw8<T>& r) {
-  uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < Raw8<T>::N; ++i) q[i] = r.v[i];
-}
-
-template <typename T>
-__device__ __forceinline__ void raw8_to_f32(const Raw8<T>& r, float (&f)[8]) {
-  const T* e = reinterpret_cast<const T*>(&r.v[0]);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) f[i] = to_f32(e[i]);
-}
-
-template <typename T>
-__device__ __forceinline__ void store_f32x8(T* p, const float (&f)[8]) {
-  Raw8<T> r;
-  T* e = reinterpret_cast<T*>(&r.v[0]);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) e[i] = from_f32<T>(f[i]);
-  store_raw8(p, r);
-}
-
 // ---- work units over variable-length rows ---------------------------------------------------
 
 // Units of one row: ceil(L / seg_len), 0 for empty or malformed rows.
