@@ -568,10 +568,17 @@ constexpr uint32_t kBufCopy = kImgBytes + 8192 + 16;
 constexpr uint32_t kSImg = 2 * kBufBytes;        // S_0 [32][128] hi, lo: 8 KiB each
 constexpr uint32_t kUImg = kSImg + 16384;        // U^T [32][64] hi, lo: 4 KiB each
 constexpr int kScanSmemNew = (int)kUImg + 8192 + 1024;
-// 8 warps: warps w and w + 4 share TMEM lane quarter w and split its 32 columns, so each phase
-// that moves the state, U or O between TMEM, registers and shared memory has half the work per
-// warp on the chunk chain
-constexpr int kScanThreads = 256;
+// kScanWpq warps share each TMEM lane quarter (warp w takes quarter w % 4) and split its 32
+// columns, so every phase that moves the state, U or O between TMEM, registers and shared memory
+// has 1 / kScanWpq of the work per warp on the chunk chain.
+#ifndef GDN_SCAN_WPQ
+#define GDN_SCAN_WPQ 2
+#endif
+constexpr int kScanWpq = GDN_SCAN_WPQ;        // 1, 2 or 4
+constexpr int kScanThreads = 128 * kScanWpq;
+constexpr int kScanCols = 32 / kScanWpq;      // TMEM columns per warp
+constexpr int kScanHalf = kScanCols / 2;      // U columns per lane (lanes 16..31 take the upper half)
+static_assert(kScanWpq == 1 || kScanWpq == 2 || kScanWpq == 4, "1, 2 or 4 warps per lane quarter");
 static_assert(kScanSmemNew <= 232448, "scan shared memory");
 
 __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const PrefillLaunch p) {
@@ -609,7 +616,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const Prefi
     if (slot >= p.num_slots) slot = 0;
     read_prior = false;
   }
-  const int wq = warp & 3, ch = warp >> 2;  // TMEM lane quarter; half of the quarter's 32 columns
+  const int wq = warp & 3, ch = warp >> 2;  // TMEM lane quarter; which kScanCols of its 32 columns
   const int dk = 32 * wq + lane;            // this thread's TMEM lane of S^T
   const int dv0 = 32 * q;
   // element (dv0 + j, dk) of the state is at base + j * kD
@@ -629,15 +636,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const Prefi
   tc::fence_after();
   // O alternates between two accumulators: chunk c's outputs are drained while chunk c + 1 runs
   const uint32_t tS = tmem_base, tU = tmem_base + 32, tO0 = tmem_base + 64, tU2 = tmem_base + 128;
-  auto store_outputs = [&](int c) {  // row t of O -> 16 bf16 of out[token][h][dv0 + 16 ch ..]
-    float o[16];
-    tc::tmem_ld16(tc::tmem_lane_col(tO0 + 32 * (c & 1), warp, 16 * ch), o);
+  auto store_outputs = [&](int c) {  // row t of O -> kScanCols bf16 of out[token][h][dv0 + ..]
+    float o[kScanCols];
+    tc::tmem_ld<kScanCols>(tc::tmem_lane_col(tO0 + 32 * (c & 1), warp, kScanCols * ch), o);
     if (lane < 16) {
       const int gt = sGt[c & 1][16 * wq + lane];
       if (gt >= 0) {
-        uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)gt * p.Hv + h) * kD + dv0 + 16 * ch);
+        uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)gt * p.Hv + h) * kD + dv0 + kScanCols * ch);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) dst[i] = tc::pack8(o + 8 * i);
+        for (int i = 0; i < kScanCols / 8; ++i) dst[i] = tc::pack8(o + 8 * i);
       }
     }
   };
@@ -663,17 +670,17 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const Prefi
   int mma_commits[5] = {0, 0, 0, 0, 0}, mma_done[5] = {0, 0, 0, 0, 0};
 
   // initial state: images of S_0 (unscaled) and gamma_0 S_0^T in TMEM
-  float v[16];
+  float v[kScanCols];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = read_prior ? gS0[(int64_t)(16 * ch + j) * kD] : 0.f;
-  tc::put_mn32_row(s_hi, s_lo, dk, v, 2 * ch, 2);
+  for (int j = 0; j < kScanCols; ++j) v[j] = read_prior ? gS0[(int64_t)(kScanCols * ch + j) * kD] : 0.f;
+  tc::put_mn32_row(s_hi, s_lo, dk, v, kScanCols / 8 * ch, kScanCols / 8);
   bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma[0], 0, p.wait_ns));
   if (ok) tma_done[0] = 1;
   if (ok) {
     const float g0 = *reinterpret_cast<const float*>(sm + kBufMeta);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] *= g0;
-    tc::tmem_st16(tc::tmem_lane_col(tS, warp, 16 * ch), v);
+    for (int j = 0; j < kScanCols; ++j) v[j] *= g0;
+    tc::tmem_st<kScanCols>(tc::tmem_lane_col(tS, warp, kScanCols * ch), v);
     tc::tmem_st_wait();
   }
   tc::fence_async_smem();
@@ -722,13 +729,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const Prefi
     ++mma_commits[4];
     if (c > 0) store_outputs(c - 1);  // while the U products run
     // this lane's U~ values (independent of the products): rows t of this warp's quarter sit in
-    // lanes 0..15 of it; of the warp's 16 columns, lanes 16..31 take over the second 8
+    // lanes 0..15 of it; of the warp's kScanCols columns, lanes 16..31 take over the upper half
     const int sh = lane >> 4, t = 16 * wq + (lane & 15);
-    float4 utv[2];
+    const int ucol = kScanCols * ch + kScanHalf * sh;  // this lane's first U column
+    float4 utv[kScanHalf / 4];
     {
-      const float4* ut = reinterpret_cast<const float4*>(buf + kBufUt) + t * 8 + 4 * ch + 2 * sh;
-      utv[0] = ut[0];
-      utv[1] = ut[1];
+      const float4* ut = reinterpret_cast<const float4*>(buf + kBufUt) + t * 8 + ucol / 4;
+#pragma unroll
+      for (int j4 = 0; j4 < kScanHalf / 4; ++j4) utv[j4] = ut[j4];
     }
     // Each warp goes on as soon as U is ready (the issuing thread's warp joins after issuing the
     // output products); the block-wide barrier comes only before the next products are issued.
@@ -739,22 +747,24 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const Prefi
     // U += U~; U^T images (row = dv, column = t)
     if (u_ok) {
       tc::fence_after();
-      float u[16], u2[16];
-      tc::tmem_ld16x2(tc::tmem_lane_col(tU, warp, 16 * ch), u, tc::tmem_lane_col(tU2, warp, 16 * ch), u2);
+      float u[kScanCols], u2[kScanCols];
+      tc::tmem_ld2<kScanCols>(tc::tmem_lane_col(tU, warp, kScanCols * ch), u,
+                              tc::tmem_lane_col(tU2, warp, kScanCols * ch), u2);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) u[j] += u2[j];
-      float w8[8];
+      for (int j = 0; j < kScanCols; ++j) u[j] += u2[j];
+      float w[kScanHalf];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float upper = __shfl_sync(0xffffffffu, u[8 + j], lane & 15);
-        w8[j] = sh ? upper : u[j];
+      for (int j = 0; j < kScanHalf; ++j) {
+        const float upper = __shfl_sync(0xffffffffu, u[kScanHalf + j], lane & 15);
+        w[j] = sh ? upper : u[j];
       }
 #pragma unroll
-      for (int j4 = 0; j4 < 2; ++j4) {
+      for (int j4 = 0; j4 < kScanHalf / 4; ++j4) {
         const float4 f = utv[j4];
-        w8[4 * j4] += f.x; w8[4 * j4 + 1] += f.y; w8[4 * j4 + 2] += f.z; w8[4 * j4 + 3] += f.w;
+        w[4 * j4] += f.x; w[4 * j4 + 1] += f.y; w[4 * j4 + 2] += f.z; w[4 * j4 + 3] += f.w;
       }
-      tc::put_mn32_row(u_hi, u_lo, t, w8, 2 * ch + sh, 1);
+      if constexpr (kScanHalf >= 8) tc::put_mn32_row(u_hi, u_lo, t, w, ucol / 8, kScanHalf / 8);
+      else tc::put_mn32_half(u_hi, u_lo, t, w, ucol / 8, (ucol / 4) & 1);
     }
     tc::fence_async_smem();
     tc::fence_before();
@@ -793,20 +803,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const Prefi
       tc::fence_after();
       // the new state: gamma_{c+1} S^T back into TMEM (in flight while the images for the next
       // chunk are written)
-      tc::tmem_ld16(tc::tmem_lane_col(tS, warp, 16 * ch), v);
+      tc::tmem_ld<kScanCols>(tc::tmem_lane_col(tS, warp, kScanCols * ch), v);
       if (c + 1 < nch) {
         const int nb = (c + 1) & 1;
         tma_ok = tc::mbar_wait(&bar_tma[nb], tma_done[nb] & 1, p.wait_ns);
         if (tma_ok) ++tma_done[nb];
         const float gn = *reinterpret_cast<const float*>(sm + nb * kBufBytes + kBufMeta);
-        float sv[16];
+        float sv[kScanCols];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) sv[j] = v[j] * gn;
-        tc::tmem_st16(tc::tmem_lane_col(tS, warp, 16 * ch), sv);
-        tc::put_mn32_row(s_hi, s_lo, dk, v, 2 * ch, 2);
+        for (int j = 0; j < kScanCols; ++j) sv[j] = v[j] * gn;
+        tc::tmem_st<kScanCols>(tc::tmem_lane_col(tS, warp, kScanCols * ch), sv);
+        tc::put_mn32_row(s_hi, s_lo, dk, v, kScanCols / 8 * ch, kScanCols / 8);
       } else if (slot > 0) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) gS[(int64_t)(16 * ch + j) * kD] = v[j];
+        for (int j = 0; j < kScanCols; ++j) gS[(int64_t)(kScanCols * ch + j) * kD] = v[j];
       }
     }
     const bool mma_ok = s_ok && tc::mbar_wait(&bar_mma[2], mma_done[2] & 1, p.wait_ns);

@@ -235,6 +235,53 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       : "memory");
 }
 
+// 8 consecutive fp32 columns of this thread's TMEM lane; two such loads with one wait; a store.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void tmem_ld8x2(uint32_t ta, float (&va)[8], uint32_t tb, float (&vb)[8]) {
+  uint32_t r[8], q[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(ta));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7])
+               : "r"(tb));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    va[j] = __uint_as_float(r[j]);
+    vb[j] = __uint_as_float(q[j]);
+  }
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+
+// N (8, 16 or 32) consecutive fp32 columns of this thread's TMEM lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 8) tmem_ld8(taddr, v);
+  else if constexpr (N == 16) tmem_ld16(taddr, v);
+  else tmem_ld32(taddr, v);
+}
+template <int N>
+__device__ __forceinline__ void tmem_ld2(uint32_t ta, float (&va)[N], uint32_t tb, float (&vb)[N]) {
+  if constexpr (N == 8) tmem_ld8x2(ta, va, tb, vb);
+  else if constexpr (N == 16) tmem_ld16x2(ta, va, tb, vb);
+  else tmem_ld32x2(ta, va, tb, vb);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -250,6 +297,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
       "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
+}
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[N]) {
+  if constexpr (N == 8) tmem_st8(taddr, v);
+  else if constexpr (N == 16) tmem_st16(taddr, v);
+  else tmem_st32(taddr, v);
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -281,6 +334,19 @@ __device__ __forceinline__ void put_mn32_row(uint8_t* hi_img, uint8_t* lo_img, i
     *reinterpret_cast<uint4*>(hi_img + off) = hi;
     *reinterpret_cast<uint4*>(lo_img + off) = lo;
   }
+}
+// 4 fp32 values of row k of the same image pair: half `hf` (0 or 1) of chunk c, 8-byte stores.
+__device__ __forceinline__ void put_mn32_half(uint8_t* hi_img, uint8_t* lo_img, int k, const float* x, int c, int hf) {
+  const int r = k & 7;
+  const uint32_t off = (uint32_t)((k >> 3) * 512 + r * 64) + ((uint32_t)(c ^ ((r >> 1) & 3)) << 4) + 8u * hf;
+  __nv_bfloat16 h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[i] = __float2bfloat16_rn(x[i]);
+    l[i] = __float2bfloat16_rn(x[i] - __bfloat162float(h[i]));
+  }
+  *reinterpret_cast<uint2*>(hi_img + off) = *reinterpret_cast<const uint2*>(h);
+  *reinterpret_cast<uint2*>(lo_img + off) = *reinterpret_cast<const uint2*>(l);
 }
 __device__ __forceinline__ uint4 pack8(const float* x) {
   __nv_bfloat16 h[8];
