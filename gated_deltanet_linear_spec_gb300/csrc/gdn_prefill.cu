@@ -300,9 +300,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       }
       sq = warp_sum32(sq);
       sk = warp_sum32(sk);
-      const float rq = 1.0f / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
+      // hardware reciprocal square root (2 ulp): well inside what the chunk products carry
+      const float rq = rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
       if (lane == 0) sRk[t] = rk;
-      const float gam = expf(sG[t]);
+      const float gam = __expf(sG[t]);  // gamma_t for the bf16 gamma q^ rows (output products only)
       float qn[4], kn[4], qg[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
