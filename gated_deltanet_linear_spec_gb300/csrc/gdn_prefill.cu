@@ -196,6 +196,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   const int64_t C = p.C;
   const int qoff = kh * kD, koff = p.Hk * kD + kh * kD, voff = 2 * p.Hk * kD + h * kD;
 
+  // the gate inputs of the chunk's tokens (threads 0 .. nc-1) go out before the row copies, so
+  // that their latency runs under the copy issue
+  float a_in = 0.f, b_in = 0.f;
+  bool has_gate = false;
+  if (tid < nc) {
+    const int gt = global_token(p.rows, bos + t0 + tid, p.num_global, p.status);
+    if (gt >= 0) {
+      a_in = __bfloat162float(static_cast<const __nv_bfloat16*>(p.a)[(int64_t)gt * p.Hv + h]);
+      b_in = __bfloat162float(static_cast<const __nv_bfloat16*>(p.b)[(int64_t)gt * p.Hv + h]);
+      has_gate = true;
+    }
+  }
+  const float a_log = __ldg(p.A_log + h), dt_b = __ldg(p.dt_bias + h);
+
   // 0. every row the chunk reads starts its trip to shared memory at once (cp.async, no
   //    registers held): the q and k rows into the image region they are turned into (one
   //    commit group), the v rows into the T / A region, which nothing uses before the first
@@ -228,14 +242,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
   // 1. gates (padded tokens: g = 0, beta = 0), TMEM and barrier
   if (tid < kCh) {
     float g = 0.f, beta = 0.f;
-    if (tid < nc) {
-      const int gt = global_token(p.rows, bos + t0 + tid, p.num_global, p.status);
-      if (gt >= 0) {
-        const __nv_bfloat16* ga = static_cast<const __nv_bfloat16*>(p.a);
-        const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.b);
-        g = gate_g(__bfloat162float(ga[(int64_t)gt * p.Hv + h]), __ldg(p.A_log + h), __ldg(p.dt_bias + h));
-        beta = 1.f / (1.f + expf(-__bfloat162float(gb[(int64_t)gt * p.Hv + h])));
-      }
+    if (has_gate) {
+      g = gate_g(a_in, a_log, dt_b);
+      beta = 1.f / (1.f + expf(-b_in));
     }
     sG[tid] = g;
     sBeta[tid] = beta;
