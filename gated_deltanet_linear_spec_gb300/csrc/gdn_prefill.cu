@@ -450,24 +450,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
       }
-      // 6a. T image (rows t, K = s): row tid % 64, columns 32 (tid / 64) .. +31
-      {
-        const int t2 = tid & 63, g0 = 32 * (tid >> 6);
-#pragma unroll
-        for (int g8 = g0; g8 < g0 + 32; g8 += 8) {
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s2 = g8 + e;
-            x[e] = s2 <= t2 ? sA[s2 * kAStride + t2] : 0.f;
-          }
-          uint4 hi, lo;
-          tc::split8(x, hi, lo);
-          const uint32_t off = tc::img_off(t2, g8, 1);
-          *reinterpret_cast<uint4*>(t_hi + off) = hi;
-          *reinterpret_cast<uint4*>(t_lo + off) = lo;
-        }
-      }
     } else {
       // 6b. meanwhile, on warps 4-7: the A operand of MMA 2, read MN-major (a [s][d] tile laid
       //     out like a K-major one): the k^ rows of the [q^; k^] images scaled in place by
@@ -498,6 +480,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
       }
       if (tid == 128) *reinterpret_cast<float*>(rec + kMeta) = expf(Gc);
     }
+    __syncthreads();
+    // 6a. T image (rows t, K = s) once the solve is done, on all eight warps: row tid % 64,
+    //     columns 16 (tid / 64) .. +15
+    {
+      const int t2 = tid & 63, g0 = 16 * (tid >> 6);
+#pragma unroll
+      for (int g8 = g0; g8 < g0 + 16; g8 += 8) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int s2 = g8 + e;
+          x[e] = s2 <= t2 ? sA[s2 * kAStride + t2] : 0.f;
+        }
+        uint4 hi, lo;
+        tc::split8(x, hi, lo);
+        const uint32_t off = tc::img_off(t2, g8, 1);
+        *reinterpret_cast<uint4*>(t_hi + off) = hi;
+        *reinterpret_cast<uint4*>(t_lo + off) = lo;
+      }
+    }
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
@@ -523,12 +525,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
     ok = __syncthreads_and(tc::mbar_wait(&bar, 1, p.wait_ns));
     if (ok) {
       tc::fence_after();
-      // 8. -W and U~ (fp32) from TMEM, lane = row d, warp w taking columns 32 (w / 4) .. +31:
-      //    -W^T row d goes straight to the record as row d of a [dk][t] image (read MN-major by
-      //    the scan), 16-byte chunks
+      // 8. -W and U~ (fp32) from TMEM, lane = row d, warp w taking columns 32 (w / 4) .. +31,
+      //    staged in shared memory exactly as the record holds them (the MMA operands there are
+      //    consumed) and stored by two bulk copies: -W^T row d as row d of a [dk][t] image (read
+      //    MN-major by the scan), U~ as [dv/32][t][32]
       const int quarter = warp & 3, half = warp >> 2;
       const int d = 32 * quarter + lane;
-      float* ut = reinterpret_cast<float*>(rec + kUt);
+      float* ut = reinterpret_cast<float*>(sm + 32768);
       float w[32];
       tc::tmem_ld32(tc::tmem_lane_col(tmem, quarter, 64 + 32 * half), w);
 #pragma unroll
@@ -539,12 +542,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(const Prefi
         uint4 hi, lo;
         tc::split8(x, hi, lo);
         const uint32_t off = tc::img_off(d, 32 * half + 8 * c, 1);
-        *reinterpret_cast<uint4*>(rec + kWnHi + off) = hi;
-        *reinterpret_cast<uint4*>(rec + kWnLo + off) = lo;
+        *reinterpret_cast<uint4*>(sm + kWnHi + off) = hi;
+        *reinterpret_cast<uint4*>(sm + kWnLo + off) = lo;
       }
       tc::tmem_ld32(tc::tmem_lane_col(tmem, quarter, 128 + 32 * half), w);
 #pragma unroll
       for (int i = 0; i < 32; ++i) ut[((d >> 5) * kCh + 32 * half + i) * 32 + (d & 31)] = w[i];
+      tc::fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc::bulk_s2g(rec + kWnHi, sm + kWnHi, 32768);
+        tc::bulk_s2g(rec + kUt, sm + 32768, 32768);
+        tc::bulk_store_commit();
+        tc::bulk_store_wait();
+      }
     }
   }
   if (!ok) {
