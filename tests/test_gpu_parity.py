@@ -4,7 +4,6 @@ Every workload runs the whole path (gdn_mixed_batch) once on the GPU and once in
 the same seeded inputs, then compares outputs and states within the stated tolerances, the conv
 ring bit for bit, and the set of written slots exactly.
 """
-import numpy as np
 import pytest
 import torch
 
