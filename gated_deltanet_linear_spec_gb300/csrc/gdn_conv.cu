@@ -73,10 +73,21 @@ __global__ void __launch_bounds__(kConvThreads, GDN_CONV_MINB) conv_update_kerne
   if (t0 >= L) return;
   const int t1 = min(L, t0 + seg_len);
 
-  if (!ct.begin(p, R, n, row, seg, t0, reporter)) return;
   YT* __restrict__ y = static_cast<YT*>(p.y[s]);
-  ct.tokens(p, R, n, row, t0, t1, reporter,
-            [&](int t, const float(&out)[kConvVE]) { store_f32v<YT, kConvVE>(y + (int64_t)(row.bos + t) * p.C + c0, out); });
+  auto sink = [&](int t, const float(&out)[kConvVE]) {
+    store_f32v<YT, kConvVE>(y + (int64_t)(row.bos + t) * p.C + c0, out);
+  };
+  if constexpr (sizeof(RawV<T, kConvVE>) == 16) {
+    if (!R.is_spec) {  // non-spec units: every input row in flight at once through shared memory
+      __shared__ RawV<T, kConvVE> stage[(kConvSegNS + W - 1) * kConvThreads];
+      if (!ct.begin_staged(p, R, n, row, seg, t0, t1, reporter, stage + threadIdx.x)) return;
+      ct.tokens_staged(t0, t1, stage + threadIdx.x, sink);
+      ct.finish(p, R, row, t1 == L);
+      return;
+    }
+  }
+  if (!ct.begin(p, R, n, row, seg, t0, reporter)) return;
+  ct.tokens(p, R, n, row, t0, t1, reporter, sink);
   ct.finish(p, R, row, t1 == L);
 }
 

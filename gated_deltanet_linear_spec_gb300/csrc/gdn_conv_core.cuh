@@ -272,6 +272,99 @@ struct ConvThread {
     }
   }
 
+  // A non-spec unit's inputs through shared memory: the W-1 window rows (the slot's history for
+  // segment 0, the previous x rows otherwise) and the unit's token rows [t0, t1) go out at once as
+  // 16-byte cp.async copies into this thread's own column of `stage` (row r at stage[r * kConvThreads]),
+  // so that no register is held while they are in flight; the window is then taken into
+  // registers.  The same slot resolution as begin() for a non-spec row.  Returns false when the
+  // row must be skipped (num_accepted out of range).
+  __device__ __forceinline__ bool begin_staged(const ConvLaunch& p, const RowsDev& R, int n, const ConvRow& row,
+                                               int seg, int t0, int t1, bool reporter, RawV<T, VE>* stage) {
+    static_assert(sizeof(RawV<T, VE>) == 16, "one 16-byte copy per row");
+    if (R.num_acc && (row.na < 1 || row.na > R.spec_cols)) {
+      if (reporter) set_status(p.status, GDN_STATUS_NUM_ACCEPTED);
+      return false;
+    }
+    per_slot = false;
+    slot = row.own;
+    int rd = row.own, anchor = 0;
+    if (R.num_acc) {  // acceptance-aware row: the history its previous verify step accepted
+      if (p.conv_layout == GDN_CONV_PER_SLOT) rd = __ldg(R.spec_idx + (int64_t)n * R.spec_cols + row.na - 1);
+      else anchor = row.na - 1;
+    }
+    bool read_prior = rd > 0 && row.has_init;
+    if (slot >= p.num_slots || rd >= p.num_slots) {
+      if (reporter) set_status(p.status, GDN_STATUS_SLOT_RANGE);
+      if (slot >= p.num_slots) slot = 0;
+      read_prior = false;
+    }
+    const T* __restrict__ x = static_cast<const T*>(p.x);
+    const T* __restrict__ pool = static_cast<const T*>(p.conv_pool);
+    xc = x_channel(p, c0);
+    const int64_t C = p.C;
+    slot_base = (int64_t)slot * p.state_len * C + c0;
+    const int64_t hist_base = (int64_t)(read_prior ? rd : 0) * p.state_len * C + c0;
+    // every token index first (no copy is issued between them), then every copy
+    constexpr int kRows = kConvSegNS + W - 1;
+    int g[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const int t = t0 - (W - 1) + r;  // token of staged row r
+      g[r] = -1;
+      if (t >= t0 ? t < t1 : seg > 0) g[r] = global_token(R, row.bos + t, p.num_global, p.status);
+    }
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const int t = t0 - (W - 1) + r;
+      const T* src = nullptr;
+      if (t < t0 && seg == 0) {
+        if (read_prior) src = pool + hist_base + (int64_t)(anchor + r) * C;
+      } else if (g[r] >= 0) {
+        src = x + (int64_t)g[r] * C + xc;
+      }
+      RawV<T, VE>* dst = stage + r * kConvThreads;
+      if (src) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                     "l"(src)
+                     : "memory");
+      } else if (t < t1) {
+        *dst = zero_rawv<T, VE>();
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < W - 1; ++i) win[i] = stage[i * kConvThreads];
+    // From here on this thread owns its slot elements: every read of them is done.
+    writer = (seg == 0 && slot > 0);
+    spec_ring = false;
+    return true;
+  }
+
+  // Tokens [ta, tb) of a unit staged by begin_staged: y_t handed to sink(t, y[VE]).
+  template <typename Sink>
+  __device__ __forceinline__ void tokens_staged(int ta, int tb, const RawV<T, VE>* stage, Sink&& sink) {
+    for (int t = ta; t < tb; ++t) {
+      const RawV<T, VE> xr = stage[(W - 1 + t - ta) * kConvThreads];
+      float hf[W - 1][VE], xf[VE], out[VE];
+#pragma unroll
+      for (int i = 0; i < W - 1; ++i) rawv_to_f32(win[i], hf[i]);
+      rawv_to_f32(xr, xf);
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        float acc = bias[e];
+#pragma unroll
+        for (int i = 0; i < W - 1; ++i) acc = fmaf(w[i][e], hf[i][e], acc);
+        acc = fmaf(w[W - 1][e], xf[e], acc);
+        out[e] = silu(acc);
+      }
+      sink(t, out);
+#pragma unroll
+      for (int i = 0; i < W - 2; ++i) win[i] = win[i + 1];
+      win[W - 2] = xr;
+    }
+  }
+
   // Non-spec rows: columns 0..W-2 <- the row's last W-1 inputs H[L..L+W-2].  `saw_end`: this
   // thread's tokens reached the row's end, so the window holds exactly those inputs.
   __device__ __forceinline__ void finish(const ConvLaunch& p, const RowsDev& R, const ConvRow& row, bool saw_end) {
