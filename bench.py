@@ -154,10 +154,43 @@ def algorithmic_bytes(batch) -> dict:
 # ------------------------------------------------------------------------------------------
 # clocks during the timed region
 
+# The sampling loop, run as a child process so that no lock of this interpreter delays it: read-only
+# NVML queries of one GPU (SM clock, its maximum, the clock-event reasons) every `period` seconds
+# on the system-wide monotonic clock, written out when the stop file appears.
+_NVML_SAMPLER = r"""
+import ctypes, os, sys, time
+uuid, index, period, out_path, stop_path = sys.argv[1], int(sys.argv[2]), float(sys.argv[3]), sys.argv[4], sys.argv[5]
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+if lib.nvmlInit_v2() != 0:
+    sys.exit(3)
+h = ctypes.c_void_p()
+if not uuid or lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+    if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+        sys.exit(4)
+reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+rows = []
+print("ready", flush=True)
+while not os.path.exists(stop_path) and len(rows) < 2000000:
+    t = time.monotonic()
+    if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and reasons(h, ctypes.byref(rs)) == 0):
+        rows.append("%.6f %d %d %d" % (t, sm.value, mx.value, rs.value))
+    time.sleep(period)
+with open(out_path, "w") as f:
+    f.write("\n".join(rows))
+lib.nvmlShutdown()
+"""
+
+
 class ClockSampler:
-    """SM clocks and clock-event (throttle) reasons sampled during the run, by read-only NVML
-    queries from a background thread every ~1 ms (nvidia-smi's 200 ms polling when the NVML
-    library cannot be loaded).  Nothing here changes a setting of the GPU."""
+    """SM clocks and clock-event (throttle) reasons sampled during the run by read-only NVML
+    queries in a child process, as fast as NVML answers (at most every 0.25 ms; on GB300 hosts
+    about every 5-10 ms, so a timed region of a few milliseconds holds one or two samples and
+    the whole run's samples are reported beside them).  A sampling thread in this interpreter
+    competed with the launching thread for the interpreter lock (1 us more per spec-verify
+    step); the child does not.  nvidia-smi's 200 ms polling when NVML cannot be loaded.  Times
+    are on the system-wide monotonic clock.  Nothing here changes a setting of the GPU."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
@@ -165,57 +198,39 @@ class ClockSampler:
                   "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                   "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, cuda_index: int, period_s: float = 0.001):
-        import threading
-        self.samples = []  # (perf_counter, sm_mhz, max_mhz, reason names)
+    def __init__(self, cuda_index: int, period_s: float = 0.00025):
+        self.samples = []  # (monotonic time, sm_mhz, max_mhz, reason names)
         self.windows = []  # (start, end) of the metric's timed region
         self.source = None
-        self._stop = threading.Event()
-        self._thread = None
+        self.period_ms = period_s * 1e3
+        self._child = None
         self._smi = None
-        dev = self._nvml_device(cuda_index)
-        if dev is not None:
-            self.source = "nvml"
-            self._thread = threading.Thread(target=self._nvml_loop, args=(dev, period_s), daemon=True)
-            self._thread.start()
-        else:
+        if not self._start_nvml(cuda_index, period_s):
             self._start_smi(cuda_index)
 
-    def _nvml_device(self, cuda_index):
-        import ctypes
+    def _start_nvml(self, cuda_index, period_s) -> bool:
+        uuid = ""
         try:
-            lib = ctypes.CDLL("libnvidia-ml.so.1")
-            if lib.nvmlInit_v2() != 0:
-                return None
-            h = ctypes.c_void_p()
-            uuid = None
-            try:
-                u = str(torch.cuda.get_device_properties(cuda_index).uuid)
-                uuid = u if u.startswith("GPU-") else "GPU-" + u
-            except Exception:
-                pass
-            if uuid is None or lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
-                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(h)) != 0:
-                    return None
-            self._lib = lib
-            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
-            return h
-        except (OSError, AttributeError):
-            return None
-
-    def _nvml_loop(self, h, period_s):
-        import ctypes
-        sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
-        while not self._stop.is_set():
-            t = time.perf_counter()
-            ok = self._lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0  # NVML_CLOCK_SM
-            ok = ok and self._lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
-            ok = ok and self._reasons_fn(h, ctypes.byref(rs)) == 0
-            if ok:
-                names = tuple(n for bit, n in self.REASONS.items() if rs.value & bit)
-                self.samples.append((t, float(sm.value), float(mx.value), names))
-            time.sleep(period_s)
+            u = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            uuid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        try:
+            self._dir = tempfile.mkdtemp(prefix="clocks")
+            self._out = os.path.join(self._dir, "samples.txt")
+            self._stopfile = os.path.join(self._dir, "stop")
+            self._child = subprocess.Popen([sys.executable, "-c", _NVML_SAMPLER, uuid, str(cuda_index), str(period_s),
+                                            self._out, self._stopfile], stdout=subprocess.PIPE,
+                                           stderr=subprocess.DEVNULL, text=True)
+            if self._child.stdout.readline().strip() != "ready":
+                self._child.wait(timeout=10)
+                self._child = None
+                return False
+            self.source = "nvml"
+            return True
+        except Exception:
+            self._child = None
+            return False
 
     def _start_smi(self, cuda_index):
         try:
@@ -224,23 +239,30 @@ class ClockSampler:
             self._smi = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
                                           "-i", str(cuda_index), "-lms", "200"], stdout=self._fh,
                                          stderr=subprocess.DEVNULL)
-            self._t0 = time.perf_counter()
+            self._t0 = time.monotonic()
             self.source = "nvidia-smi"
         except Exception:
             self._smi = None
 
     def mark(self, start: float, end: float) -> None:
-        """Records one timed region (perf_counter times taken after the synchronizes around it)."""
+        """Records one timed region (time.monotonic() taken after the synchronizes around it)."""
         self.windows.append((start, end))
 
     def stop(self) -> dict:
-        if self._thread is not None:
-            self._stop.set()
-            self._thread.join(timeout=5)
+        if self._child is not None:
+            open(self._stopfile, "w").close()
             try:
-                self._lib.nvmlShutdown()
+                self._child.wait(timeout=20)
+                with open(self._out) as f:
+                    for line in f:
+                        parts = line.split()
+                        if len(parts) != 4:
+                            continue
+                        bits = int(parts[3])
+                        names = tuple(n for bit, n in self.REASONS.items() if bits & bit)
+                        self.samples.append((float(parts[0]), float(parts[1]), float(parts[2]), names))
             except Exception:
-                pass
+                self._child.kill()
         elif self._smi is not None:
             self._smi.terminate()
             try:
@@ -270,7 +292,7 @@ class ClockSampler:
                 "samples_whole_run": len(self.samples),
                 "sm_mhz_whole_run": statistics.median(s[1] for s in self.samples) if self.samples else None,
                 "reasons_whole_run": sorted({r for s in self.samples for r in s[3]}),
-                "source": self.source, "period_ms": 1.0 if self.source == "nvml" else 200.0}
+                "source": self.source, "period_ms": self.period_ms if self.source == "nvml" else 200.0}
 
 
 # ------------------------------------------------------------------------------------------
@@ -650,10 +672,10 @@ def main() -> int:
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    t_region0 = time.perf_counter()
+    t_region0 = time.monotonic()
     step_ms = timed_rotating(step_fns, steps, flush, stream)
     torch.cuda.synchronize()
-    clocks.mark(t_region0, time.perf_counter())
+    clocks.mark(t_region0, time.monotonic())
     if dist:
         dist.barrier()
 
