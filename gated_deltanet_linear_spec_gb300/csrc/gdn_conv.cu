@@ -18,7 +18,9 @@
 // 16-token segments for parallelism; segment 0 alone touches the slot (it fetches the row's last
 // W-1 inputs for the write-back when the row is longer than one segment), later segments rebuild
 // their window from x.  All accesses are 16-byte vectors along the channel axis (8 bf16 or
-// 2x4 fp32 per thread); the token index and x loads of 4 tokens are issued together.
+// 2x4 fp32 per thread).  A spec unit issues the token index and x loads of 4 tokens together;
+// a non-spec unit of bf16 activations issues every window and token row of the thread's column
+// at once as cp.async copies into shared memory (no register held while they are in flight).
 // The kernel lets the dependent recurrence grid launch early (programmatic dependent launch):
 // that grid only reads this kernel's output after griddepcontrol.wait.
 #include "gdn_conv_core.cuh"
