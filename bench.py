@@ -169,12 +169,13 @@ if not uuid or lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 
         sys.exit(4)
 reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
 sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:  # the maximum does not change
+    sys.exit(5)
 rows = []
 print("ready", flush=True)
 while not os.path.exists(stop_path) and len(rows) < 2000000:
     t = time.monotonic()
-    if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and
-            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and reasons(h, ctypes.byref(rs)) == 0):
+    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and reasons(h, ctypes.byref(rs)) == 0:
         rows.append("%.6f %d %d %d" % (t, sm.value, mx.value, rs.value))
     time.sleep(period)
 with open(out_path, "w") as f:
@@ -186,8 +187,8 @@ lib.nvmlShutdown()
 class ClockSampler:
     """SM clocks and clock-event (throttle) reasons sampled during the run by read-only NVML
     queries in a child process, as fast as NVML answers (at most every 0.25 ms; on GB300 hosts
-    about every 5-10 ms, so a timed region of a few milliseconds holds one or two samples and
-    the whole run's samples are reported beside them).  A sampling thread in this interpreter
+    with the GPU busy about every 5-10 ms, so a timed region of a few milliseconds holds one or
+    two samples and the whole run's samples are reported beside them).  A sampling thread in this interpreter
     competed with the launching thread for the interpreter lock (1 us more per spec-verify
     step); the child does not.  nvidia-smi's 200 ms polling when NVML cannot be loaded.  Times
     are on the system-wide monotonic clock.  Nothing here changes a setting of the GPU."""
