@@ -600,6 +600,8 @@ constexpr int kScanThreads = 128 * kScanWpq;
 constexpr int kScanCols = 32 / kScanWpq;      // TMEM columns per warp
 constexpr int kScanHalf = kScanCols / 2;      // U columns per lane (lanes 16..31 take the upper half)
 static_assert(kScanWpq == 1 || kScanWpq == 2 || kScanWpq == 4, "1, 2 or 4 warps per lane quarter");
+constexpr int kTokFirst = kScanThreads >= 256 ? kScanThreads - kCh : 96;  // first token-loading thread
+static_assert(kTokFirst > 64, "the product issuers (threads 0, 32, 64) load no token index");
 static_assert(kScanSmemNew <= 232448, "scan shared memory");
 
 __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const PrefillLaunch p) {
@@ -711,9 +713,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) chunk_scan_kernel(const Prefi
   for (int c = 0; c < nch && ok; ++c) {
     const int b = c & 1;
     uint8_t* buf = sm + b * kBufBytes;
-    if (tid < kCh) {
-      const int t = c * kCh + tid;
-      sGt[b][tid] = t < L ? global_token(p.rows, bos + t, p.num_global, p.status) : -1;
+    // the chunk's global tokens, loaded by the last warps (none of which issues products, so a
+    // gathered row's index loads never hold the products behind them)
+    for (int i = tid - kTokFirst; i >= 0 && i < kCh; i += kScanThreads - kTokFirst) {
+      const int t = c * kCh + i;
+      sGt[b][i] = t < L ? global_token(p.rows, bos + t, p.num_global, p.status) : -1;
     }
     const uint32_t tO = tO0 + 32 * b;
     // U = -W S_0^T (three passes) -> commit (thread 0);  O = (gamma q^) S_0^T -> commit (thread 32)
